@@ -1,0 +1,315 @@
+"""Pins for the CPU oracle: what the pages print, closed forms, invariants and
+brute force.  None of these re-type the oracle's own code path; each is built so
+that a plausible slip (wrong index, dropped scale, transposed K/V, wrong KV-head
+mapping, off-by-one context, missing causal limit) fails at least one test.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+
+
+def _bf16_bits(x):
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (test helper, storage form)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def _place(contig, table, num_blocks, block_size):
+    """Put a contiguous [L, Hkv, D] array into a fresh pool by the block table's
+    meaning: logical block i holds tokens [iB, (i+1)B) and lives in physical
+    block table[i].  Written with numpy block views, not with slot arithmetic."""
+    L, H, D = contig.shape
+    pool = np.full((num_blocks, block_size, H, D), np.nan, dtype=contig.dtype) if contig.dtype == np.float32 \
+        else np.zeros((num_blocks, block_size, H, D), dtype=contig.dtype)
+    for i, pb in enumerate(table):
+        chunk = contig[i * block_size:(i + 1) * block_size]
+        pool[pb, : chunk.shape[0]] = chunk
+    return pool
+
+
+# ------------------------------------------------------------------ golden
+def test_worked_example_block_count_and_ranges(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "worked_example_b16.json")))
+    B, L = g["block_size"], g["seq_len"]
+    assert oracle.num_blocks(L, B) == g["num_blocks"]
+    assert oracle.num_blocks(g["len17"]["seq_len"], B) == g["len17"]["num_blocks"]
+    assert g["len17"]["seq_len"] - (g["len17"]["num_blocks"] - 1) * B == g["len17"]["tokens_in_last_block"]
+    # every token of the 40-token sequence resolves to the printed block and its offset in it
+    table = np.array([g["block_table"]], dtype=np.int32)
+    pos = np.arange(L, dtype=np.int32)
+    slots, err = oracle.slot_mapping(table, np.zeros(L, np.int32), pos, B, 16)
+    assert err == 0
+    for (lo, hi), pb in zip(g["valid_token_ranges"], g["block_table"]):
+        for tok in range(lo, hi + 1):
+            assert slots[tok] // B == pb and slots[tok] % B == tok - lo
+    # the third block's capacity range 32..47 all lands in physical block 15
+    cap_lo, cap_hi = g["capacity_token_ranges"][2]
+    s, err = oracle.slot_mapping(table, np.zeros(cap_hi - cap_lo + 1, np.int32),
+                                 np.arange(cap_lo, cap_hi + 1, dtype=np.int32), B, 16)
+    assert err == 0 and np.all(s // B == 15) and list(s % B) == list(range(B))
+    # token 33 -> logical block 2, offset 1 -> physical block 15
+    s33, _ = oracle.slot_mapping(table, [0], [33], B, 16)
+    assert (s33[0] // B, s33[0] % B) == (15, 1)
+
+
+def test_tail_waste_bound(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "worked_example_b16.json")))
+    B = g["block_size"]
+    wastes = [oracle.num_blocks(L, B) * B - L for L in range(1, 5 * B + 3)]
+    assert max(wastes) == g["max_tail_waste"] and min(wastes) == 0
+    ex = g["kv_tokens_example"]
+    assert ex["prompt"] + ex["generated"] == ex["total"]
+    assert oracle.num_blocks(ex["total"], B) * B - ex["total"] <= g["max_tail_waste"]
+    r = g["reservation_example"]
+    assert r["reserved"] - r["used"] == r["wasted"]
+    assert oracle.num_blocks(r["used"], B) * B - r["used"] < r["wasted"]
+
+
+# ------------------------------------------------------- slot mapping / write
+@pytest.mark.parametrize("B", [1, 2, 4, 16])
+def test_slot_write_brute_force(B):
+    """Every placement of up to 3 logical blocks in a 4-block pool, every length:
+    writing a labelled contiguous sequence through the oracle's slot mapping and
+    KV write must give the block-view placement."""
+    P, H, D = 4, 2, 3
+    for nblk in range(0, 4):
+        for table in itertools.permutations(range(P), nblk):
+            for L in range(max(0, (nblk - 1) * B + 1), nblk * B + 1):
+                contig = (np.arange(L * H * D, dtype=np.float32) + 1).reshape(L, H, D)
+                bt = np.array([list(table) + [-1] * (3 - nblk)], dtype=np.int32)
+                slots, err = oracle.slot_mapping(bt, np.zeros(L, np.int32), np.arange(L, dtype=np.int32), B, P)
+                assert err == 0
+                kc = np.full((P, B, H, D), np.nan, np.float32)
+                vc = np.full((P, B, H, D), np.nan, np.float32)
+                assert oracle.write_kv(contig, -contig, kc, vc, slots) == 0
+                want = _place(contig, table, P, B)
+                np.testing.assert_array_equal(kc, want)
+                np.testing.assert_array_equal(vc, np.where(np.isnan(want), np.nan, -want))
+                assert len(set(slots.tolist())) == L  # distinct slots for distinct tokens
+
+
+def test_slot_mapping_padding_and_errors():
+    bt = np.array([[3, -1], [0, 1]], dtype=np.int32)
+    seq = np.array([0, 0, 1, 1, 0, 2, -1, 1], np.int32)
+    pos = np.array([5, -1, 9, 20, 17, 0, 0, 40], np.int32)
+    slots, err = oracle.slot_mapping(bt, seq, pos, 16, 4)
+    # 5 -> block 3 off 5; pad; 9 -> block 0 off 9; 20 -> block 1 off 4;
+    # 17 -> table entry -1 (error); seq 2 and -1 out of range (errors); 40 -> logical 2 >= width (error)
+    assert slots.tolist() == [53, -1, 9, 20, -1, -1, -1, -1]
+    assert err == 4
+
+
+def test_write_kv_skips_negative_and_rejects_out_of_pool():
+    kc = np.zeros((2, 4, 1, 2), np.float32)
+    vc = np.zeros_like(kc)
+    kn = np.ones((3, 1, 2), np.float32)
+    err = oracle.write_kv(kn, 2 * kn, kc, vc, np.array([-1, 5, 8], np.int64))
+    assert err == 1
+    assert kc.reshape(8, 2)[5].tolist() == [1, 1] and vc.reshape(8, 2)[5].tolist() == [2, 2]
+    assert np.count_nonzero(kc) == 2
+
+
+# ------------------------------------------------------------- attention
+def _decode_single(q, kc_contig, vc_contig, B, P, scale, seed=0, dtype=np.float32):
+    """One sequence, one head group: scatter contiguous K/V to a random placement and decode."""
+    L = kc_contig.shape[0]
+    nblk = oracle.num_blocks(L, B)
+    rng = np.random.default_rng(seed)
+    table = rng.permutation(P)[:nblk]
+    kp = _place(kc_contig, table, P, B)
+    vp = _place(vc_contig, table, P, B)
+    if dtype == np.float32:
+        kp = np.nan_to_num(kp, nan=1e30)  # unused slots hold huge values a correct oracle never reads
+        vp = np.nan_to_num(vp, nan=1e30)
+    bt = np.array([list(table) + [-1]], dtype=np.int32)
+    return oracle.decode(q[None], kp, vp, bt, np.array([L], np.int32), scale)[0]
+
+
+def test_single_token_returns_its_value():
+    D = 8
+    q = RNG.standard_normal((1, D)).astype(np.float32)
+    k = RNG.standard_normal((1, 1, D)).astype(np.float32)
+    v = RNG.standard_normal((1, 1, D)).astype(np.float32)
+    o = _decode_single(q, k, v, 16, 4, 0.3)
+    np.testing.assert_array_equal(o[0], v[0, 0].astype(np.float64))
+
+
+def test_two_token_closed_form():
+    # x0 = 0.5 * (1*2 + 0*0) = 1, x1 = 0: weights e/(1+e) and 1/(1+e) (the logistic function)
+    q = np.array([[1.0, 0.0]], np.float32)
+    k = np.array([[[2.0, 0.0]], [[0.0, 0.0]]], np.float32)
+    v = np.array([[[1.0, 0.0]], [[0.0, 1.0]]], np.float32)
+    o = _decode_single(q, k, v, 1, 5, 0.5)[0]
+    w0 = 1.0 / (1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(o, [w0, 1.0 - w0], rtol=0, atol=1e-15)
+    # swapping the roles of K and V must change the answer (guards a transposed operand)
+    o_swapped = _decode_single(q, v, k, 1, 5, 0.5)[0]
+    assert not np.allclose(o_swapped, o)
+
+
+def test_equal_keys_and_zero_scale_give_mean():
+    L, D = 37, 16
+    q = RNG.standard_normal((1, D)).astype(np.float32)
+    v = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    k_same = np.repeat(RNG.standard_normal((1, 1, D)).astype(np.float32), L, axis=0)
+    mean = v[:, 0].astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(_decode_single(q, k_same, v, 16, 8, 0.7)[0], mean, atol=1e-12)
+    k = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    np.testing.assert_allclose(_decode_single(q, k, v, 4, 12, 0.0)[0], mean, atol=1e-12)
+
+
+def test_dominant_key_selects_its_value():
+    L, D = 20, 8
+    k = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    v = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    q = k[13].copy() * 4
+    o = _decode_single(q, k, v, 4, 8, 100.0)[0]
+    np.testing.assert_allclose(o, v[13, 0], atol=1e-9)
+
+
+def test_placement_order_shift_and_linearity_invariants():
+    L, D = 45, 16
+    q = RNG.standard_normal((1, D)).astype(np.float32)
+    k = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    v = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    base = _decode_single(q, k, v, 16, 8, 0.25, seed=1)
+    # placement: different block size and different random tables give the same answer
+    for B, P, seed in [(1, 64, 2), (4, 20, 3), (16, 5, 4)]:
+        np.testing.assert_allclose(_decode_single(q, k, v, B, P, 0.25, seed=seed), base, rtol=0, atol=1e-13)
+    # token order does not matter for decode (no positional term)
+    perm = RNG.permutation(L)
+    np.testing.assert_allclose(_decode_single(q, k[perm], v[perm], 16, 8, 0.25), base, atol=1e-13)
+    # adding one vector to every key shifts all scores equally
+    u = RNG.standard_normal((1, 1, D)).astype(np.float32)
+    shifted = (k.astype(np.float64) + u).astype(np.float32)
+    ref = _decode_single(q, shifted, v, 16, 8, 0.25)
+    # compare against the unshifted result computed on keys with the same fp32 rounding error budget
+    np.testing.assert_allclose(ref, base, atol=1e-5)
+    # linear in V
+    v2 = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    o2 = _decode_single(q, k, v2, 16, 8, 0.25)
+    o12 = _decode_single(q, k, (v.astype(np.float64) + v2).astype(np.float32), 16, 8, 0.25)
+    np.testing.assert_allclose(o12, base + o2, atol=1e-6)
+
+
+def test_independent_contiguous_attention():
+    """Paged == contiguous: a second, numpy-only fp64 computation on the contiguous
+    tensor (no block table involved) agrees with the oracle on a random placement."""
+    L, D = 100, 32
+    q = RNG.standard_normal((1, D)).astype(np.float32)
+    k = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    v = RNG.standard_normal((L, 1, D)).astype(np.float32)
+    s = 0.3 * (k[:, 0].astype(np.float64) @ q[0].astype(np.float64))
+    w = np.exp(s - s.max())
+    ref = (w[:, None] * v[:, 0].astype(np.float64)).sum(0) / w.sum()
+    np.testing.assert_allclose(_decode_single(q, k, v, 16, 16, 0.3)[0], ref, atol=1e-12)
+
+
+def test_gqa_head_mapping_and_context_length():
+    """Query head h reads KV head h // G; exactly context_len tokens are read."""
+    N, Hq, Hkv, D, B, P = 3, 6, 2, 4, 4, 10
+    G = Hq // Hkv
+    kc = RNG.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    vc = RNG.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    bt = np.array([[7, 1, -1], [2, -1, -1], [5, 9, 3]], np.int32)
+    ctx = np.array([1, 1, 1], np.int32)
+    q = RNG.standard_normal((N, Hq, D)).astype(np.float32)
+    o = oracle.decode(q, kc, vc, bt, ctx, 0.5)
+    for s in range(N):
+        for h in range(Hq):
+            np.testing.assert_array_equal(o[s, h], vc[bt[s, 0], 0, h // G].astype(np.float64))
+    # equal keys within each sequence: output = mean of exactly ctx values
+    kc2 = np.ones_like(kc)
+    ctx = np.array([6, 3, 9], np.int32)
+    o = oracle.decode(q, kc2, vc, bt, ctx, 0.5)
+    for s in range(N):
+        rows = [vc[bt[s, j // B], j % B] for j in range(ctx[s])]
+        for h in range(Hq):
+            want = np.mean([r[h // G] for r in rows], axis=0, dtype=np.float64)
+            np.testing.assert_allclose(o[s, h], want, atol=1e-12)
+
+
+def test_empty_context_is_zero_and_bad_table_rejected():
+    kc = np.zeros((2, 4, 1, 2), np.float32)
+    q = np.ones((1, 1, 2), np.float32)
+    o = oracle.decode(q, kc, kc, np.array([[-1]], np.int32), np.array([0], np.int32), 1.0)
+    assert np.all(o == 0)
+    with pytest.raises(ValueError):
+        oracle.decode(q, kc, kc, np.array([[-1]], np.int32), np.array([1], np.int32), 1.0)
+    with pytest.raises(ValueError):
+        oracle.decode(q, kc, kc, np.array([[0]], np.int32), np.array([5], np.int32), 1.0)
+
+
+def test_bf16_widening_exact():
+    vals = np.array([1.0, -2.0, 1.5, 0.0, 3.140625, -0.0078125, 65280.0, 1e-3], np.float32)
+    bits = _bf16_bits(vals)
+    assert bits[:3].tolist() == [0x3F80, 0xC000, 0x3FC0]
+    D = vals.shape[0]
+    v = bits.reshape(1, 1, D)
+    k = np.zeros((1, 1, D), np.uint16)
+    q = np.zeros((1, 1, D), np.uint16)
+    kp = np.zeros((2, 1, 1, D), np.uint16)
+    vp = np.zeros((2, 1, 1, D), np.uint16)
+    kp[1] = k
+    vp[1] = v
+    o = oracle.decode(q, kp, vp, np.array([[1]], np.int32), np.array([1], np.int32), 1.0)
+    np.testing.assert_array_equal(o[0, 0], oracle.bf16_bits_to_f64(bits))
+    assert o[0, 0, 0] == 1.0 and o[0, 0, 1] == -2.0 and o[0, 0, 2] == 1.5
+
+
+# --------------------------------------------------------------- prefill
+def _prefill_case(seed=0, B=4, Hq=4, Hkv=2, D=8):
+    rng = np.random.default_rng(seed)
+    P = 40
+    kc = rng.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    vc = rng.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    perm = rng.permutation(P)
+    bt = np.full((2, 12), -1, np.int32)
+    bt[0, :10] = perm[:10]
+    bt[1, :6] = perm[10:16]
+    ctx = np.array([37, 21], np.int32)
+    q_start = np.array([30, 0], np.int32)  # chunk 0: positions 30..36 of seq 0; chunk 1: 0..20 of seq 1
+    cu = np.array([0, 7, 28], np.int32)
+    q = rng.standard_normal((28, Hq, D)).astype(np.float32)
+    return q, cu, q_start, np.array([0, 1], np.int32), kc, vc, bt, ctx
+
+
+def test_prefill_matches_decode_on_truncated_context():
+    q, cu, qs, soc, kc, vc, bt, ctx = _prefill_case()
+    o = oracle.prefill(q, cu, qs, soc, kc, vc, bt, ctx, 0.35)
+    for c in range(2):
+        for i in range(cu[c + 1] - cu[c]):
+            p = qs[c] + i
+            row = cu[c] + i
+            d = oracle.decode(q[row][None], kc, vc, bt[soc[c]][None], np.array([p + 1], np.int32), 0.35)
+            np.testing.assert_allclose(o[row], d[0], rtol=0, atol=1e-14)
+
+
+def test_prefill_first_position_and_causal_limit():
+    q, cu, qs, soc, kc, vc, bt, ctx = _prefill_case(seed=1)
+    o = oracle.prefill(q, cu, qs, soc, kc, vc, bt, ctx, 0.35)
+    G = q.shape[1] // kc.shape[2]
+    # chunk 1 starts at position 0: its first query sees only token 0, output = v_0 exactly
+    for h in range(q.shape[1]):
+        np.testing.assert_array_equal(o[cu[1], h], vc[bt[1, 0], 0, h // G].astype(np.float64))
+    # changing K/V of future tokens (positions > p) does not change query p
+    kc2, vc2 = kc.copy(), vc.copy()
+    B = kc.shape[1]
+    for j in range(31, 37):  # seq 0, positions 31..36 (future of query at 30)
+        kc2[bt[0, j // B], j % B] += 5.0
+        vc2[bt[0, j // B], j % B] -= 3.0
+    o2 = oracle.prefill(q, cu, qs, soc, kc2, vc2, bt, ctx, 0.35)
+    np.testing.assert_array_equal(o2[0], o[0])
+    assert not np.allclose(o2[1], o[1])
+    # a chunk that ends beyond the sequence's context is rejected
+    with pytest.raises(ValueError):
+        oracle.prefill(q, cu, qs, soc, kc, vc, bt, np.array([36, 21], np.int32), 0.35)
