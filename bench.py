@@ -1,0 +1,386 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: slot mapping and KV
+write for every new token of the step, then paged decode (and, for the mixed
+workload, causal chunked prefill).  Default workload: 64 decode sequences,
+32 query / 8 KV heads, head_dim 128, block_size 16, context lengths U[128,4096],
+bf16, random non-contiguous block tables.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0).  ``value`` is decode tokens/s (one token per
+sequence per step) over all ranks; the roofline object describes the decode
+kernel (algorithmic K/V bytes per launch / its CUDA-event time, against the
+measured HBM copy bandwidth).  L2 is flushed (a 512 MiB write) before every
+timed step.  Under torchrun each rank runs an independent replica with its
+own seed (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV-read GB/s (% of HBM peak) and decode tokens/s on 1 GB300"
+DEFAULT_WORKLOAD = "decode_bf16"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in sorted(files):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_sha256_16") == source_digest(d["source_files"]):
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        window = [p for t, p in self.samples if t0 <= t <= t1]
+        scope = "timed"
+        if len(window) < 3:
+            window = [p for t, p in self.samples if t <= t1 + 1.0]
+            scope = "run"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in window if num(p[0]) is not None]
+        mx = [num(p[1]) for p in window if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in window for n, v in zip(names, p[4:8]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(window), "window": scope}
+
+
+def decode_algorithmic_bytes(w) -> int:
+    """Bytes the decode kernel must move: K and V of every valid context token,
+    the queries and outputs, the block-table entries in use and the lengths."""
+    nd = w.num_decode
+    ctx = [int(x) for x in w.context_lens[:nd]]
+    kv = sum(ctx) * w.kv_bytes_per_token()
+    qo = 2 * nd * w.num_q_heads * w.head_dim * w.elem_bytes
+    tables = sum(-(-L // w.block_size) for L in ctx) * 4 + nd * 4
+    return kv + qo + tables
+
+
+def prefill_flops(w) -> float:
+    """Causal attention flops of the chunks: 4*D*Hq per (query, visible key)."""
+    tot = 0
+    for c in range(w.num_chunks):
+        n = int(w.cu_q_lens[c + 1] - w.cu_q_lens[c])
+        off = int(w.q_start_pos[c])
+        tot += n * off + n * (n + 1) // 2
+    return 4.0 * w.head_dim * w.num_q_heads * tot
+
+
+def step_input_tensors(step):
+    """The per-step inputs a serving loop hands to the path (the pools are resident state)."""
+    return [step.q_decode, step.k_new, step.v_new, step.block_tables, step.context_lens, step.seq_idx, step.pos,
+            step.q_prefill, step.cu_q_lens, step.q_start_pos, step.seq_of_chunk]
+
+
+# ---------------------------------------------------------- CPU oracle arm
+def oracle_step_time(w, target_seconds: float):
+    """Time the oracle's full step (slot mapping, KV write, decode, prefill) on
+    the host cores, repeating until target_seconds of CPU time have passed."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_313_gb300.workloads import storage_numpy
+
+    threads = os.cpu_count() or 1
+    bt = w.block_tables.numpy()
+    kc0 = storage_numpy(w.k_cache)
+    vc0 = storage_numpy(w.v_cache)
+    args = dict(kn=storage_numpy(w.k_new), vn=storage_numpy(w.v_new), qd=storage_numpy(w.q_decode),
+                qp=storage_numpy(w.q_prefill))
+    kc, vc = kc0.copy(), vc0.copy()
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        slots, _ = oracle.slot_mapping(bt, w.seq_idx.numpy(), w.pos.numpy(), w.block_size, w.num_blocks)
+        oracle.write_kv(args["kn"], args["vn"], kc, vc, slots)
+        nd = w.num_decode
+        if nd:
+            oracle.decode(args["qd"], kc, vc, bt[:nd], w.context_lens.numpy()[:nd], w.scale, num_threads=threads)
+        if w.num_chunks:
+            oracle.prefill(args["qp"], w.cu_q_lens.numpy(), w.q_start_pos.numpy(), w.seq_of_chunk.numpy(), kc, vc, bt,
+                           w.context_lens.numpy(), w.scale, num_threads=threads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= target_seconds or len(times) >= 1000:
+            break
+    del np
+    return statistics.mean(times), len(times), threads
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_313_gb300 import workloads as W
+
+    w = W.make(args.workload, args.seed)
+    steps = max(1, args.steps)
+    # every step is one oracle pass over the full workload; bounded so the run ends within minutes
+    budget = min(max(args.cpu_seconds, 1.0), 120.0)
+    per_step, n, threads = oracle_step_time(w, budget / max(1, min(steps, 4)))
+    tokens = w.num_decode
+    value = tokens / per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} full oracle steps of workload {w.name} (fp64 C, {threads} threads)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    ctx = [int(x) for x in w.context_lens[: w.num_decode]]
+    cfg = {"workload": w.name, "decode_seqs": w.num_decode, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+           "head_dim": w.head_dim, "block_size": w.block_size, "num_blocks": w.num_blocks,
+           "sum_context_tokens": sum(ctx), "max_context": max(ctx) if ctx else 0,
+           "prefill_chunks": w.num_chunks, "prefill_queries": int(w.cu_q_lens[-1]) if w.num_chunks else 0,
+           "new_tokens": int(w.seq_idx.numel()), "seed": w.meta.get("seed", 0),
+           "l2": "flushed before every timed step (512 MiB write)"}
+    return cfg
+
+
+# ------------------------------------------------------------- native arm
+def run_native(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from paged_kv_cache_313_gb300 import pa
+    from paged_kv_cache_313_gb300 import workloads as W
+    from paged_kv_cache_313_gb300.runner import DeviceStep
+
+    pa.lib()  # fail loudly if the CUDA library is missing
+    w = W.make(args.workload, args.seed + rank)
+    step = DeviceStep(w, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = 2 + (1 if w.num_decode else 0) + (1 if w.num_chunks else 0)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        step.run()
+    barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = visible.split(",")[local].strip() if visible else str(local)
+    sampler = ClockSampler(smi_index)
+    time.sleep(0.3)
+    barrier()
+    t0 = time.time()
+    for i in range(K):
+        e = ev[i]
+        flush.fill_(i & 0xFF)
+        e[0].record(stream)
+        step.slot_mapping()
+        step.write_kv()
+        e[1].record(stream)
+        step.decode()
+        e[2].record(stream)
+        step.prefill()
+        e[3].record(stream)
+    barrier()
+    t1 = time.time()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    prefill_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
+
+    # end to end through the public API: pinned host inputs -> device, step, output -> host
+    host_in = [t.detach().cpu().pin_memory() for t in step_input_tensors(step)]
+    host_out_d = torch.empty(step.out_decode.shape, dtype=step.out_decode.dtype).pin_memory()
+    host_out_p = torch.empty(step.out_prefill.shape, dtype=step.out_prefill.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out_d.numel() * host_out_d.element_size() + host_out_p.numel() * host_out_p.element_size()
+    e2e_ms = []
+    K2 = max(1, min(K, 50))
+    for i in range(K2):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for dst, src in zip(step_input_tensors(step), host_in):
+            dst.copy_(src, non_blocking=True)
+        step.run()
+        host_out_d.copy_(step.out_decode, non_blocking=True)
+        host_out_p.copy_(step.out_prefill, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    sampler.stop()
+    errors = step.errors()
+
+    mean_step = statistics.mean(step_ms)
+    mean_dec = statistics.mean(decode_ms)
+    mean_e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([mean_step, mean_dec, mean_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_step, mean_dec, mean_e2e = t.tolist()
+
+    hbm, bf16_tf, bf16_tf_sus, peak_kind = peaks()
+    alg_bytes = decode_algorithmic_bytes(w)
+    achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
+    tokens = w.num_decode * world
+    value = tokens / (mean_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
+                       / (mean_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "pa_decode", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "algorithmic_bytes_per_launch": alg_bytes, "ms_per_launch": mean_dec,
+                     "traffic": recorded_traffic("pa_decode", w.name)},
+        "stage_ms": {"slot_mapping+write_kv": statistics.mean(write_ms), "decode": mean_dec,
+                     "prefill": statistics.mean(prefill_ms)},
+        "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2},
+        "gpu_launches": K * launches_per_step,
+        "clocks": sampler.summary(t0, t1),
+        "device_errors": errors,
+    }
+    if w.num_chunks:
+        fl = prefill_flops(w)
+        pm = statistics.mean(prefill_ms)
+        line["prefill"] = {"flops_per_launch": fl, "ms_per_launch": pm, "achieved_tflops": fl / (pm * 1e-3) / 1e12,
+                           "peak_tflops": bf16_tf, "frac": fl / (pm * 1e-3) / 1e12 / bf16_tf}
+    if rank == 0 and not args.no_cpu_baseline:
+        per, n, threads = oracle_step_time(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": w.num_decode / per, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} full oracle steps of workload {w.name} (fp64 C, {threads} threads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

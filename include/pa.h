@@ -1,0 +1,193 @@
+/*
+ * pa.h — C ABI of libpa.so, the GB300 (sm_103a) paged-attention hot path.
+ *
+ * Sources (page title, then section):
+ *   [P1] "什么是 PagedAttention？"
+ *   [P2] "PagedAttention学习笔记"
+ *   [P3] "KV cache 显存管理：为什么 PagedAttention 是 vLLM 的核心"
+ *
+ * The operation: the KV cache lives in fixed-size physical blocks of
+ * block_size (B) token slots; each sequence's block table maps its logical
+ * block i (tokens iB .. iB+B-1) to a physical block ([P2] §2.1; [P3]
+ * "分页思想：逻辑连续，物理不连续").  New tokens are scattered to
+ * slot = physical_block * B + pos % B ([P2] 代码实现部分 › BlockTable), and
+ * attention gathers K/V through the table: logical_block = pos / B,
+ * offset = pos % B, physical = block_table[seq][logical_block] ([P3]
+ * "PagedAttention 改变了什么"), computing the unchanged softmax(scale QK^T)V
+ * ([P2] "与 FlashAttention 的关系").  The argument list follows the kernel
+ * inputs of [P3] "对 ModelRunner 的影响": the new tokens, each sequence's
+ * context length and block table, the physical block pool and the write slots.
+ *
+ * Conventions for every entry point:
+ *  - Tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *    row-major.  The library allocates no device memory; scratch comes from
+ *    the caller's workspace.
+ *  - K and V pools are separate arrays laid out [num_blocks][block_size]
+ *    [num_kv_heads][head_dim]: element (slot, h, d) is at
+ *    (slot*num_kv_heads + h)*head_dim + d.  Query head h reads KV head
+ *    h / (num_q_heads / num_kv_heads).
+ *  - Block tables are int32 [num_seqs][max_blocks_per_seq]; entries past a
+ *    sequence's last block are ignored (conventionally -1).
+ *  - context_lens[s] counts every token sequence s attends to, including the
+ *    token(s) written in the same step (write first, then attend).
+ *  - dtype is PA_F32 or PA_BF16 and applies to q, k/v (new and pooled) and out.
+ *  - stream is a cudaStream_t passed as void*; NULL means the legacy default
+ *    stream.  All calls are asynchronous on that stream.
+ *  - Return value: PA_OK, or an error status; nothing is launched when the
+ *    host-side checks fail.  PA_ERR_CUDA carries the CUDA error code in
+ *    pa_last_cuda_error() (per calling thread).
+ *  - Optional error_count (device int32, may be NULL): kernels add the number
+ *    of invalid indices they met (out-of-range sequence, logical block, table
+ *    entry or slot).  Invalid entries are skipped, never dereferenced.
+ *  - The device must be compute capability 10.3 (GB300); otherwise
+ *    PA_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,        /* null pointer, negative size, inconsistent shape */
+    PA_ERR_UNSUPPORTED = 2,        /* head_dim / block_size / group size / dtype not built */
+    PA_ERR_CUDA = 3,               /* a CUDA runtime call failed, see pa_last_cuda_error() */
+    PA_ERR_WORKSPACE = 4,          /* workspace missing or smaller than required */
+    PA_ERR_UNSUPPORTED_DEVICE = 5  /* current device is not sm_103 */
+};
+
+enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 };
+
+/* Library ABI version (major*100 + minor). */
+PA_API int pa_version(void);
+
+/* Static, human-readable name of a status code. */
+PA_API const char* pa_status_string(int status);
+
+/* cudaError_t of the last PA_ERR_CUDA returned on this thread (0 if none). */
+PA_API int pa_last_cuda_error(void);
+
+/*
+ * Slot mapping ([P2] 代码实现部分 › "块表与槽位映射：BlockTable",
+ * compute_slot_mapping; [P2] 三、算法流程与数据结构).
+ * For each new token t of sequence seq_idx[t] at position pos[t]:
+ *     slot_mapping[t] = block_tables[seq_idx[t]][pos[t] / B] * B + pos[t] % B
+ * pos[t] < 0 marks padding: slot -1, not an error ([P2] writes -1 for tokens
+ * another rank owns).  An out-of-range sequence, a logical block at or beyond
+ * max_blocks_per_seq, or a table entry outside [0, num_blocks) gives slot -1
+ * and counts one error.
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]   (read)
+ *   seq_idx, pos  int32 [num_tokens]                     (read)
+ *   slot_mapping  int64 [num_tokens]                     (written)
+ * num_tokens == 0 is a no-op.  block_size >= 1.
+ */
+PA_API int pa_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                    const int32_t* seq_idx, const int32_t* pos, int num_tokens, int block_size,
+                    int num_blocks, int64_t* slot_mapping, int32_t* error_count, void* stream);
+
+/*
+ * Paged KV write ([P3] "对 ModelRunner 的影响": the slot says where the
+ * current token's K/V is written).  Bit-exact copy:
+ *     k_cache[slot_mapping[t]] = k_new[t],  v_cache[slot_mapping[t]] = v_new[t]
+ * for every t with slot_mapping[t] >= 0; a row is num_kv_heads*head_dim
+ * elements.  Slots at or beyond num_blocks*block_size count one error and
+ * are skipped.  Slots must be distinct (the same slot twice is a race).
+ *   k_new, v_new      [num_tokens][num_kv_heads][head_dim]            (read)
+ *   k_cache, v_cache  [num_blocks][block_size][num_kv_heads][head_dim] (written at the slots)
+ * Needs num_kv_heads*head_dim*sizeof(dtype) to be a multiple of 16 bytes and
+ * all four arrays 16-byte aligned, else PA_ERR_UNSUPPORTED.
+ */
+PA_API int pa_write_kv(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads, int head_dim,
+                int dtype, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                const int64_t* slot_mapping, int32_t* error_count, void* stream);
+
+/*
+ * Bytes of workspace pa_decode needs for these sizes (split-KV partial
+ * results plus one ticket counter per (sequence, kv head)).  Deterministic:
+ * the same arguments on the same device always give the same size.
+ */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_context_len);
+
+/*
+ * Paged decode attention, one query token per sequence ([P2] 三、算法流程与
+ * 数据结构: the kernel reads Q and the block table, gathers K/V block by
+ * block, then softmax(QK^T)V; [P3] "PagedAttention 改变了什么" for the
+ * address chain).  For sequence s and query head h, with L = context_lens[s]
+ * and kv = h / (num_q_heads/num_kv_heads):
+ *     out[s][h] = sum_{j<L} softmax_j(scale * q[s][h] . K[s][j][kv]) V[s][j][kv]
+ * where K[s][j] is pool row block_tables[s][j/B]*B + j%B.  L == 0 gives zeros.
+ *   out, q        [num_seqs][num_q_heads][head_dim]   (out written, q read)
+ *   context_lens  int32 [num_seqs]; every entry must be <= max_context_len
+ *                 and <= max_blocks_per_seq*B (larger entries are clamped and
+ *                 counted as errors; pass error_count to see them)
+ * Long contexts are split into partitions processed in parallel and merged
+ * with a log-sum-exp combine in a fixed order (deterministic).  workspace must
+ * hold pa_decode_workspace_size(...) bytes, be 256-byte aligned, and be zeroed
+ * once before its first use; the library leaves it zeroed-for-reuse after
+ * every call.  One workspace must not serve two calls that may overlap on the
+ * GPU.  Supported: head_dim 64 or 128, block_size 8..128 dividing 64 or a
+ * multiple of 64, num_q_heads/num_kv_heads in 1..16.
+ */
+PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+              int dtype, const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int max_context_len, float scale, void* workspace, size_t workspace_bytes,
+              int32_t* error_count, void* stream);
+
+/*
+ * Causal chunked-prefill attention over the paged pool ([P1] 工作原理:
+ * prefill takes blocks for the input length; the chunk's own K/V are written
+ * by pa_write_kv first).  Chunk c holds queries cu_q_lens[c] ..
+ * cu_q_lens[c+1]-1 of sequence seq_of_chunk[c]; query i of the chunk sits at
+ * absolute position p = q_start_pos[c] + i and attends keys 0..p of that
+ * sequence through its block table:
+ *     out[r][h] = sum_{j<=p} softmax_j(scale * q[r][h] . K[j][kv]) V[j][kv]
+ * Needs q_start_pos[c] + n_c <= context_lens[seq_of_chunk[c]] (else the
+ * chunk is clamped and counted as an error).
+ *   out, q        [total_q][num_q_heads][head_dim]
+ *   cu_q_lens     int32 [num_chunks+1], cu_q_lens[0] = 0, nondecreasing,
+ *                 cu_q_lens[num_chunks] = total_q; max_q_len bounds n_c
+ *   q_start_pos, seq_of_chunk  int32 [num_chunks]
+ * workspace: pa_prefill_workspace_size(...) bytes (may be 0, then NULL is fine).
+ */
+PA_API size_t pa_prefill_workspace_size(int num_chunks, int max_q_len, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size);
+
+PA_API int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                     const int32_t* seq_of_chunk, int num_chunks, int total_q, int max_q_len,
+                     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int dtype,
+                     const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+                     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                     float scale, void* workspace, size_t workspace_bytes, int32_t* error_count,
+                     void* stream);
+
+/*
+ * Copy-on-write block copy ([P1] 共享但不污染状态: a write into a shared
+ * partial block first copies its valid entries into a private block).  For
+ * each i < num_copies, token slots 0..num_valid[i]-1 of physical block
+ * src_blocks[i] are copied to dst_blocks[i], in both pools.  Destinations
+ * must be distinct and must not be sources.  Out-of-range blocks or
+ * num_valid outside [0, block_size] count one error and are skipped.
+ *   src_blocks, dst_blocks, num_valid  int32 [num_copies]  (device, read)
+ */
+PA_API int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int num_kv_heads,
+                   int head_dim, int dtype, const int32_t* src_blocks, const int32_t* dst_blocks,
+                   const int32_t* num_valid, int num_copies, int32_t* error_count, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

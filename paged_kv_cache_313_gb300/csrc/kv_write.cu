@@ -1,0 +1,120 @@
+// kv_write.cu — the write side of the paged cache: slot mapping, the slot-
+// mapped K/V scatter and the copy-on-write block copy.
+//
+// Slot mapping follows "PagedAttention学习笔记", 代码实现部分 › BlockTable
+// (compute_slot_mapping): slot = block_table[seq][pos / B] * B + pos % B, -1 for
+// tokens that are not written.  The scatter follows "KV cache 显存管理：为什么
+// PagedAttention 是 vLLM 的核心", 对 ModelRunner 的影响 (the slot says where the
+// current token's K/V goes).  The block copy follows "什么是 PagedAttention？",
+// 共享但不污染状态 (copy the valid entries of a shared partial block).
+//
+// All three are pure data movement: HBM-bound, 16-byte vector accesses, no
+// shared-memory staging needed since every byte is touched exactly once.
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int num_seqs, int max_blocks_per_seq,
+                                    const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos,
+                                    int num_tokens, int block_size, int num_blocks, int64_t* __restrict__ slots,
+                                    int32_t* error_count) {
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= num_tokens) return;
+    int p = pos[t];
+    long long slot = -1;
+    if (p >= 0) {
+        int s = seq_idx[t];
+        int logical_block = p / block_size;
+        int offset = p - logical_block * block_size;
+        bool ok = s >= 0 && s < num_seqs && logical_block < max_blocks_per_seq;
+        if (ok) {
+            int physical = block_tables[(long long)s * max_blocks_per_seq + logical_block];
+            ok = physical >= 0 && physical < num_blocks;
+            if (ok) slot = (long long)physical * block_size + offset;
+        }
+        if (!ok) count_error(error_count);
+    }
+    slots[t] = slot;
+}
+
+// One CTA per token: its K row and V row (row_bytes each, a multiple of 16)
+// are copied with 16-byte loads and stores.
+__global__ void write_kv_kernel(const int4* __restrict__ k_new, const int4* __restrict__ v_new, int row_vecs,
+                                int4* __restrict__ k_cache, int4* __restrict__ v_cache, long long num_slots,
+                                const int64_t* __restrict__ slots, int32_t* error_count) {
+    int t = blockIdx.x;
+    long long slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) count_error(error_count);
+        return;
+    }
+    const int4* ks = k_new + (long long)t * row_vecs;
+    const int4* vs = v_new + (long long)t * row_vecs;
+    int4* kd = k_cache + slot * row_vecs;
+    int4* vd = v_cache + slot * row_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        int4 k = __ldg(ks + i);
+        int4 v = __ldg(vs + i);
+        kd[i] = k;
+        vd[i] = v;
+    }
+}
+
+// One CTA per copy: num_valid token rows of the source block, both pools.
+__global__ void copy_blocks_kernel(int4* __restrict__ k_cache, int4* __restrict__ v_cache, int num_blocks,
+                                   int block_size, int row_vecs, const int32_t* __restrict__ src,
+                                   const int32_t* __restrict__ dst, const int32_t* __restrict__ num_valid,
+                                   int32_t* error_count) {
+    int c = blockIdx.x;
+    int s = src[c], d = dst[c], n = num_valid[c];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || n < 0 || n > block_size) {
+        if (threadIdx.x == 0) count_error(error_count);
+        return;
+    }
+    long long block_vecs = (long long)block_size * row_vecs;
+    long long count = (long long)n * row_vecs;
+    const int4* ks = k_cache + s * block_vecs;
+    const int4* vs = v_cache + s * block_vecs;
+    int4* kd = k_cache + d * block_vecs;
+    int4* vd = v_cache + d * block_vecs;
+    for (long long i = threadIdx.x; i < count; i += blockDim.x) {
+        kd[i] = ks[i];
+        vd[i] = vs[i];
+    }
+}
+
+}  // namespace
+
+int launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks_per_seq, const int32_t* seq_idx,
+                        const int32_t* pos, int num_tokens, int block_size, int num_blocks, int64_t* slot_mapping,
+                        int32_t* error_count, cudaStream_t stream) {
+    const int threads = 256;
+    slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0, stream>>>(
+        block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, num_tokens, block_size, num_blocks, slot_mapping,
+        error_count);
+    return check_launch();
+}
+
+int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
+                    void* v_cache, long long num_slots, const int64_t* slot_mapping, int32_t* error_count,
+                    cudaStream_t stream) {
+    int row_vecs = row_bytes / 16;
+    int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
+    write_kv_kernel<<<num_tokens, threads, 0, stream>>>(
+        static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs, static_cast<int4*>(k_cache),
+        static_cast<int4*>(v_cache), num_slots, slot_mapping, error_count);
+    return check_launch();
+}
+
+int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,
+                       const int32_t* src, const int32_t* dst, const int32_t* num_valid, int num_copies,
+                       int32_t* error_count, cudaStream_t stream) {
+    copy_blocks_kernel<<<num_copies, 256, 0, stream>>>(static_cast<int4*>(k_cache), static_cast<int4*>(v_cache),
+                                                       num_blocks, block_size, row_bytes / 16, src, dst, num_valid,
+                                                       error_count);
+    return check_launch();
+}
+
+}  // namespace pa

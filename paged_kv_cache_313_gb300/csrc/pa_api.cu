@@ -1,0 +1,285 @@
+// pa_api.cu — the C ABI of libpa.so: argument checks, device checks and
+// dispatch to the kernels.  Every entry point validates on the host and
+// launches nothing when a check fails.
+#include <cstdio>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+static thread_local int g_last_cuda_error = 0;
+
+int set_cuda_error(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return PA_ERR_CUDA;
+}
+
+int check_launch() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PA_OK : set_cuda_error(e);
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int checked = 0;  // 0 unknown, 1 ok, -1 not sm_103
+    int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+}  // namespace
+
+int check_device(int* num_sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    DeviceInfo& info = g_devices[dev];
+    if (info.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return set_cuda_error(e);
+        info.checked = (major == 10 && minor == 3) ? 1 : -1;
+        info.num_sms = sms;
+    }
+    if (num_sms) *num_sms = info.num_sms;
+    return info.checked == 1 ? PA_OK : PA_ERR_UNSUPPORTED_DEVICE;
+}
+
+int ensure_dynamic_smem(const void* kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev})) return PA_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    done.insert({kernel, dev});
+    return PA_OK;
+}
+
+DecodePlan plan_decode(int num_seqs, int num_kv_heads, int max_context_len, int num_sms) {
+    // 512-token partitions keep each CTA's stream of K/V long enough to hide
+    // the pipeline fill; shrink them while the grid would not cover two waves
+    // of the GPU; grow them so that no (sequence, head) has more than 128
+    // partials to merge.
+    int partition = 512;
+    auto ctas = [&](int part) {
+        long long splits = (max_context_len + part - 1) / part;
+        return (long long)num_seqs * num_kv_heads * (splits < 1 ? 1 : splits);
+    };
+    while (partition > 64 && ctas(partition) < 2LL * num_sms) partition >>= 1;
+    while ((max_context_len + partition - 1) / partition > 128) partition <<= 1;
+    int splits = (max_context_len + partition - 1) / partition;
+    return DecodePlan{partition, splits < 1 ? 1 : splits};
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_splits) {
+    DecodeWorkspace w;
+    size_t units = (size_t)num_seqs * num_kv_heads;
+    size_t group = (size_t)(num_q_heads / num_kv_heads);
+    w.counters = 0;
+    w.ml = align_up(units * sizeof(int), 256);
+    w.o = align_up(w.ml + units * max_splits * group * sizeof(float2), 256);
+    w.total = align_up(w.o + units * max_splits * group * head_dim * sizeof(float), 256);
+    return w;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+        default: return "unknown status";
+    }
+}
+
+int pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pa_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks_per_seq, const int32_t* seq_idx,
+                    const int32_t* pos, int num_tokens, int block_size, int num_blocks, int64_t* slot_mapping,
+                    int32_t* error_count, void* stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 0 || block_size < 1 || num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!seq_idx || !pos || !slot_mapping || (num_seqs > 0 && max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_INVALID_ARG;
+    int rc = check_device(nullptr);
+    if (rc != PA_OK) return rc;
+    return launch_slot_mapping(block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, num_tokens, block_size,
+                               num_blocks, slot_mapping, error_count, static_cast<cudaStream_t>(stream));
+}
+
+int pa_write_kv(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads, int head_dim, int dtype,
+                void* k_cache, void* v_cache, int num_blocks, int block_size, const int64_t* slot_mapping,
+                int32_t* error_count, void* stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || num_blocks < 0 || block_size < 1)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    long long row_bytes = (long long)num_kv_heads * head_dim * elem_size(dtype);
+    if (row_bytes % 16 != 0 || row_bytes > (1 << 20)) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_UNSUPPORTED;
+    int rc = check_device(nullptr);
+    if (rc != PA_OK) return rc;
+    return launch_write_kv(k_new, v_new, num_tokens, (int)row_bytes, k_cache, v_cache,
+                           (long long)num_blocks * block_size, slot_mapping, error_count,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                   int dtype, const int32_t* src_blocks, const int32_t* dst_blocks, const int32_t* num_valid,
+                   int num_copies, int32_t* error_count, void* stream) {
+    if (num_copies < 0 || num_blocks < 0 || block_size < 1 || num_kv_heads < 1 || head_dim < 1)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_copies == 0) return PA_OK;
+    if (!k_cache || !v_cache || !src_blocks || !dst_blocks || !num_valid) return PA_ERR_INVALID_ARG;
+    long long row_bytes = (long long)num_kv_heads * head_dim * elem_size(dtype);
+    if (row_bytes % 16 != 0 || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_UNSUPPORTED;
+    int rc = check_device(nullptr);
+    if (rc != PA_OK) return rc;
+    return launch_copy_blocks(k_cache, v_cache, num_blocks, block_size, (int)row_bytes, src_blocks, dst_blocks,
+                              num_valid, num_copies, error_count, static_cast<cudaStream_t>(stream));
+}
+
+static int decode_shape_ok(int num_q_heads, int num_kv_heads, int head_dim, int block_size) {
+    if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size < 1 || block_size > 1024) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_context_len) {
+    if (num_seqs < 0 || max_context_len < 0 || decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size))
+        return 0;
+    int num_sms = 0;
+    if (check_device(&num_sms) != PA_OK) return 0;
+    DecodePlan plan = plan_decode(num_seqs, num_kv_heads, max_context_len, num_sms);
+    return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total;
+}
+
+int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int dtype,
+              const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int max_context_len, float scale, void* workspace, size_t workspace_bytes, int32_t* error_count,
+              void* stream) {
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PA_OK) return rc;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_INVALID_ARG;
+    int num_sms = 0;
+    if ((rc = check_device(&num_sms)) != PA_OK) return rc;
+    DecodePlan plan = plan_decode(num_seqs, num_kv_heads, max_context_len, num_sms);
+    DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.error_count = error_count;
+    p.counters = reinterpret_cast<int*>(ws + lay.counters);
+    p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
+    p.ws_o = reinterpret_cast<float*>(ws + lay.o);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.group = num_q_heads / num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_context_len = max_context_len;
+    p.partition = plan.partition;
+    p.max_splits = plan.max_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, static_cast<cudaStream_t>(stream));
+    return launch_decode_fma(p, dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_prefill_workspace_size(int num_chunks, int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size) {
+    (void)num_chunks; (void)max_q_len; (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size;
+    return 0;
+}
+
+int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                     const int32_t* seq_of_chunk, int num_chunks, int total_q, int max_q_len, int num_seqs,
+                     int num_q_heads, int num_kv_heads, int head_dim, int dtype, const void* k_cache,
+                     const void* v_cache, int num_blocks, int block_size, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* context_lens, float scale, void* workspace,
+                     size_t workspace_bytes, int32_t* error_count, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    if (num_chunks < 0 || total_q < 0 || max_q_len < 0 || num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PA_OK) return rc;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_chunks == 0 || total_q == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !q || !cu_q_lens || !q_start_pos || !seq_of_chunk || !k_cache || !v_cache || !context_lens ||
+        !block_tables || num_seqs == 0)
+        return PA_ERR_INVALID_ARG;
+    if ((rc = check_device(nullptr)) != PA_OK) return rc;
+    PrefillParams p;
+    p.out = out;
+    p.q = q;
+    p.cu_q_lens = cu_q_lens;
+    p.q_start_pos = q_start_pos;
+    p.seq_of_chunk = seq_of_chunk;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.error_count = error_count;
+    p.num_chunks = num_chunks;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.group = num_q_heads / num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    return launch_prefill_fma(p, dtype, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

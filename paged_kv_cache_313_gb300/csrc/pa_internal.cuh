@@ -1,0 +1,121 @@
+// pa_internal.cuh — shared declarations of the libpa.so translation units:
+// status plumbing, device properties, launch parameter structs and small
+// device helpers.  Not part of the public ABI (that is include/pa.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- host side
+int set_cuda_error(cudaError_t e);  // records e for pa_last_cuda_error(), returns PA_ERR_CUDA
+int check_launch();                 // PA_OK or PA_ERR_CUDA after a kernel launch
+int check_device(int* num_sms);     // PA_OK on an sm_103 device (cached per device)
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (once per kernel and device).
+int ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+inline int elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+// Split-KV partition policy shared by pa_decode and pa_decode_workspace_size.
+struct DecodePlan {
+    int partition;   // tokens per split (multiple of 64)
+    int max_splits;  // ceil(max_context_len / partition)
+};
+DecodePlan plan_decode(int num_seqs, int num_kv_heads, int max_context_len, int num_sms);
+
+// Workspace layout of pa_decode (byte offsets from the 256-aligned base).
+struct DecodeWorkspace {
+    size_t counters;  // int32 [num_seqs][num_kv_heads]
+    size_t ml;        // float2 [num_seqs][num_kv_heads][max_splits][G]  (running max in log2 units, sum)
+    size_t o;         // float  [num_seqs][num_kv_heads][max_splits][G][head_dim]
+    size_t total;
+};
+DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_splits);
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* error_count;
+    int* counters;
+    float2* ws_ml;
+    float* ws_o;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
+    int num_blocks, block_size, max_blocks_per_seq, max_context_len;
+    int partition, max_splits;
+    float scale_log2;  // scale * log2(e): scores are kept in base-2 units
+};
+
+struct PrefillParams {
+    void* out;
+    const void* q;
+    const int32_t* cu_q_lens;
+    const int32_t* q_start_pos;
+    const int32_t* seq_of_chunk;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* error_count;
+    int num_chunks, total_q, max_q_len, num_seqs;
+    int num_q_heads, num_kv_heads, head_dim, group;
+    int num_blocks, block_size, max_blocks_per_seq;
+    float scale_log2;
+};
+
+// Kernel launchers (defined in the .cu files).
+int launch_prefill_fma(const PrefillParams& p, int dtype, cudaStream_t stream);
+int launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_blocks_per_seq, const int32_t* seq_idx,
+                        const int32_t* pos, int num_tokens, int block_size, int num_blocks, int64_t* slot_mapping,
+                        int32_t* error_count, cudaStream_t stream);
+int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
+                    void* v_cache, long long num_slots, const int64_t* slot_mapping, int32_t* error_count,
+                    cudaStream_t stream);
+int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,
+                       const int32_t* src, const int32_t* dst, const int32_t* num_valid, int num_copies,
+                       int32_t* error_count, cudaStream_t stream);
+int launch_decode_fma(const DecodeParams& p, int dtype, cudaStream_t stream);
+bool decode_tc_supported(const DecodeParams& p, int dtype);
+int launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ float from_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);  // round to nearest even
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void count_error(int32_t* error_count, int n = 1) {
+    if (error_count != nullptr && n != 0) atomicAdd(error_count, n);
+}
+
+// Number of token partitions of a context of length L (>= 1 so that an empty
+// context still has one owner that writes its zero output).
+__device__ __forceinline__ int num_partitions(int L, int partition) {
+    return L <= 0 ? 1 : (L + partition - 1) / partition;
+}
+
+}  // namespace pa

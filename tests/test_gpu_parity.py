@@ -1,0 +1,201 @@
+"""GPU parity of the hot path against the CPU oracle, through the C ABI.
+
+Bit-exact: slot mapping, KV write (whole pools compared), copy-on-write copy.
+Attention: max-abs error against the fp64 oracle, 1e-5 for fp32 and 2e-2 for
+bf16 workloads.  Reduced workloads span several partitions, tiles and ragged
+tails; the full workloads are the ones the benchmark times, in the same
+launch configuration.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_313_gb300 import pa
+from paged_kv_cache_313_gb300 import workloads as W
+from paged_kv_cache_313_gb300.allocator import BlockAllocator
+from paged_kv_cache_313_gb300.runner import DeviceStep
+from paged_kv_cache_313_gb300.workloads import storage_numpy
+
+from oracle_step import expected_step
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2}
+
+_cache = {}
+
+
+def _case(kind, name):
+    key = (kind, name)
+    if key not in _cache:
+        w = W.make(name, 0) if kind == "full" else W.small(name, 0)
+        _cache.clear()  # keep one large workload resident at a time
+        _cache[key] = (w, expected_step(w))
+    return _cache[key]
+
+
+CASES = [("small", n) for n in ("tiny_fp32", "decode_bf16", "longctx_bf16", "shared_prefix_bf16", "mixed_bf16")] + \
+        [("full", n) for n in ("decode_bf16", "longctx_bf16", "shared_prefix_bf16", "shared_prefix_cow_bf16",
+                               "mixed_bf16")]
+
+
+def _maxabs(got: torch.Tensor, want: np.ndarray) -> float:
+    g = got.float().cpu().double().numpy()
+    assert np.all(np.isfinite(g))
+    return float(np.max(np.abs(g - want))) if want.size else 0.0
+
+
+@pytest.mark.parametrize("kind,name", CASES)
+def test_step_parity(kind, name):
+    w, exp = _case(kind, name)
+    st = DeviceStep(w)
+    st.slot_mapping()
+    assert torch.equal(st.slots.cpu(), torch.from_numpy(exp.slots)), "slot mapping differs"
+    st.write_kv()
+    kc = storage_numpy(st.k_cache.cpu())
+    vc = storage_numpy(st.v_cache.cpu())
+    assert np.array_equal(kc, exp.k_cache) and np.array_equal(vc, exp.v_cache), "pool contents differ after write"
+    out_d = st.decode()
+    if w.num_decode:
+        err = _maxabs(out_d, exp.out_decode)
+        assert err <= TOL[w.dtype], f"decode max-abs error {err}"
+    if w.num_chunks:
+        out_p = st.prefill()
+        err = _maxabs(out_p, exp.out_prefill)
+        assert err <= TOL[w.dtype], f"prefill max-abs error {err}"
+    torch.cuda.synchronize()
+    assert st.errors() == 0
+
+
+@pytest.mark.parametrize("name", ["decode_bf16", "mixed_bf16"])
+def test_repeat_runs_bitwise_identical(name):
+    w, _ = _case("small", name)
+    st = DeviceStep(w)
+    a = [t.clone() for t in st.run()]
+    for _ in range(3):
+        b = st.run()
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+def test_slot_mapping_invalid_entries_match_oracle():
+    bt = np.array([[3, -1], [0, 1]], dtype=np.int32)
+    seq = np.array([0, 0, 1, 1, 0, 2, -1, 1], np.int32)
+    pos = np.array([5, -1, 9, 20, 17, 0, 0, 40], np.int32)
+    want, nerr = oracle.slot_mapping(bt, seq, pos, 16, 4)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pa.pa_slot_mapping(torch.from_numpy(bt).cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda(),
+                             16, 4, error_count=err)
+    assert got.cpu().tolist() == want.tolist()
+    assert int(err.item()) == nerr == 4
+
+
+def test_write_kv_skips_padding_and_rejects_out_of_pool():
+    kc = torch.zeros(2, 4, 2, 8, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kn = torch.ones(3, 2, 8, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv(kn, 2 * kn, kc, vc, torch.tensor([-1, 5, 8], device="cuda"), error_count=err)
+    assert int(err.item()) == 1
+    assert torch.count_nonzero(kc).item() == 16 and torch.all(kc.view(8, 16)[5] == 1)
+    assert torch.all(vc.view(8, 16)[5] == 2)
+
+
+def test_copy_blocks_matches_host_copy():
+    g = torch.Generator().manual_seed(5)
+    kc = torch.randn(12, 16, 8, 128, generator=g).to(torch.bfloat16)
+    vc = torch.randn(12, 16, 8, 128, generator=g).to(torch.bfloat16)
+    src, dst, nv = [3, 7, 0], [9, 1, 5], [2, 16, 0]
+    want_k, want_v = kc.clone(), vc.clone()
+    for s, d, n in zip(src, dst, nv):
+        want_k[d, :n] = kc[s, :n]
+        want_v[d, :n] = vc[s, :n]
+    dk, dv = kc.cuda(), vc.cuda()
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device="cuda")  # noqa: E731
+    pa.pa_copy_blocks(dk, dv, i32(src), i32(dst), i32(nv))
+    assert torch.equal(dk.cpu(), want_k) and torch.equal(dv.cpu(), want_v)
+
+
+def _decode_direct(q, kc, vc, bt, ctx, max_ctx, scale, err=None):
+    ws = pa.new_decode_workspace(q.shape[0], q.shape[1], kc.shape[2], q.shape[2], kc.shape[1], max_ctx)
+    return pa.pa_decode(q, kc, vc, bt, ctx, max_ctx, scale, ws, error_count=err)
+
+
+def test_long_single_sequence_fp32_many_partitions():
+    """One fp32 sequence long enough to be split into many partitions: the
+    cross-partition merge must keep fp32 accuracy."""
+    rng = np.random.default_rng(11)
+    L, B, Hq, Hkv, D = 9000, 16, 8, 2, 64
+    nblk = oracle.num_blocks(L, B)
+    P = nblk + 17
+    table = rng.permutation(P)[:nblk].astype(np.int32)[None]
+    kc = rng.standard_normal((P, B, Hkv, D), dtype=np.float32)
+    vc = rng.standard_normal((P, B, Hkv, D), dtype=np.float32)
+    q = rng.standard_normal((1, Hq, D), dtype=np.float32)
+    want = oracle.decode(q, kc, vc, table, np.array([L], np.int32), 0.125)
+    got = _decode_direct(*(torch.from_numpy(x).cuda() for x in (q, kc, vc, table, np.array([L], np.int32))), L, 0.125)
+    assert _maxabs(got, want) <= 1e-5
+
+
+def test_empty_and_single_token_contexts():
+    rng = np.random.default_rng(3)
+    P, B, Hq, Hkv, D = 8, 16, 8, 2, 128
+    kc = rng.standard_normal((P, B, Hkv, D), dtype=np.float32)
+    vc = rng.standard_normal((P, B, Hkv, D), dtype=np.float32)
+    q = rng.standard_normal((3, Hq, D), dtype=np.float32)
+    bt = np.array([[4, -1], [-1, -1], [2, 6]], np.int32)
+    ctx = np.array([1, 0, 17], np.int32)
+    want = oracle.decode(q, kc, vc, bt, ctx, 0.1)
+    for dt in (torch.float32, torch.bfloat16):
+        t = lambda x: torch.from_numpy(x).to(dt).cuda()  # noqa: E731
+        got = _decode_direct(t(q), t(kc), t(vc), torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), 17, 0.1)
+        assert torch.all(got[1] == 0)
+        if dt == torch.float32:
+            assert _maxabs(got, want) <= 1e-5
+            assert torch.equal(got[0].cpu(), torch.from_numpy(vc[4, 0]).repeat_interleave(4, 0))
+
+
+def test_invalid_table_entries_are_skipped_and_counted():
+    rng = np.random.default_rng(4)
+    P, B, Hq, Hkv, D = 8, 16, 4, 4, 64
+    kc = torch.from_numpy(rng.standard_normal((P, B, Hkv, D), dtype=np.float32)).cuda()
+    q = torch.from_numpy(rng.standard_normal((2, Hq, D), dtype=np.float32)).cuda()
+    bt = torch.tensor([[1, -1, 99], [2, 3, 4]], dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([40, 200], dtype=torch.int32, device="cuda")  # seq 1 exceeds its table: clamped
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _decode_direct(q, kc, kc, bt, ctx, 48, 0.1, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) > 0
+    assert torch.all(torch.isfinite(out))
+
+
+def test_shared_prefix_branches_identical_after_device_cow():
+    """Two branches share a 2050-token prefix whose last block is partial; the
+    first branch's write copies it on the device (pa_copy_blocks).  With equal
+    new tokens and equal queries both branches must give identical outputs."""
+    B, Hq, Hkv, D = 16, 32, 8, 128
+    alloc = BlockAllocator(200, B, seed=9)
+    root = alloc.allocate(2050)
+    b1, b2 = alloc.fork(root), alloc.fork(root)
+    alloc.free(root)
+    copies = alloc.append(b1, 1) + alloc.append(b2, 1)
+    assert len(copies) == 1 and copies[0].num_valid == 2
+    g = torch.Generator().manual_seed(2)
+    kc = torch.randn(200, B, Hkv, D, generator=g).to(torch.bfloat16).cuda()
+    vc = torch.randn(200, B, Hkv, D, generator=g).to(torch.bfloat16).cuda()
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device="cuda")  # noqa: E731
+    pa.pa_copy_blocks(kc, vc, i32([c.src for c in copies]), i32([c.dst for c in copies]),
+                      i32([c.num_valid for c in copies]))
+    bt = torch.from_numpy(alloc.block_table([b1, b2])).cuda()
+    assert not torch.equal(bt[0], bt[1])  # the tails live in different physical blocks
+    seq_idx, pos = i32([0, 1]), i32([2050, 2050])
+    kn = torch.randn(1, Hkv, D, generator=g).to(torch.bfloat16).cuda().repeat(2, 1, 1)
+    vn = torch.randn(1, Hkv, D, generator=g).to(torch.bfloat16).cuda().repeat(2, 1, 1)
+    slots = pa.pa_slot_mapping(bt, seq_idx, pos, B, 200)
+    pa.pa_write_kv(kn, vn, kc, vc, slots)
+    q = torch.randn(1, Hq, D, generator=g).to(torch.bfloat16).cuda().repeat(2, 1, 1)
+    out = _decode_direct(q, kc, vc, bt, i32([2051, 2051]), 2051, 1 / math.sqrt(D))
+    assert torch.equal(out[0], out[1])
