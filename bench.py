@@ -257,12 +257,12 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    from paged_kv_cache_313_gb300 import pa
+    from paged_kv_cache_313_gb300 import pa, sharding
     from paged_kv_cache_313_gb300 import workloads as W
     from paged_kv_cache_313_gb300.runner import DeviceStep
 
     pa.lib()  # fail loudly if the CUDA library is missing
-    w = W.make(args.workload, args.seed + rank)
+    w = W.make(args.workload, sharding.shard_seed(args.seed, rank))
     step = DeviceStep(w, dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -327,18 +327,13 @@ def run_native(args):
     sampler.stop()
     errors = step.errors()
 
-    mean_step = statistics.mean(step_ms)
-    mean_dec = statistics.mean(decode_ms)
-    mean_e2e = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([mean_step, mean_dec, mean_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_step, mean_dec, mean_e2e = t.tolist()
+    mean_step, mean_dec, mean_e2e = sharding.max_over_ranks(
+        [statistics.mean(step_ms), statistics.mean(decode_ms), statistics.mean(e2e_ms)], device=dev)
 
     hbm, bf16_tf, bf16_tf_sus, peak_kind = peaks()
     alg_bytes = decode_algorithmic_bytes(w)
     achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
-    tokens = w.num_decode * world
+    tokens = sharding.total_units(w.num_decode)
     value = tokens / (mean_step * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
