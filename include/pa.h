@@ -147,6 +147,35 @@ PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, in
               int32_t* error_count, void* stream);
 
 /*
+ * pa_decode for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this is a deployment aid, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc where decode runs (a runtime that
+ * forbids allocation after start-up, a plugin living inside another
+ * framework's memory budget, or a caller that must not trigger the implicit
+ * synchronisation an allocation can cause).  This entry point computes
+ * exactly what pa_decode computes, with the same arguments minus the
+ * workspace: its split-KV scratch is a fixed 16 MiB array in device global
+ * memory owned by the library, which every GPU that loads the library keeps
+ * until the process exits.  It allocates nothing (no cudaMalloc / cudaFree,
+ * no allocating library routine).
+ *  - Sizes whose pa_decode_workspace_size(...) exceeds 16 MiB are rejected
+ *    with PA_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress) and caches it; make that first call before
+ *    any stream capture on the device.
+ *  - The array is shared by every call and keeps the last call's contents;
+ *    each call clears its ticket counters (an asynchronous memset on
+ *    `stream`) before launching.  Calls that may overlap on the GPU (other
+ *    streams, other host threads) race on the array: serialise them.
+ */
+PA_API int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads,
+                             int head_dim, int dtype, const void* k_cache, const void* v_cache, int num_blocks,
+                             int block_size, const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int max_context_len, float scale,
+                             int32_t* error_count, void* stream);
+
+/*
  * Causal chunked-prefill attention over the paged pool ([P1] 工作原理:
  * prefill takes blocks for the input length; the chunk's own K/V are written
  * by pa_write_kv first).  Chunk c holds queries cu_q_lens[c] ..

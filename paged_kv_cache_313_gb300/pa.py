@@ -19,8 +19,8 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_decode_workspace_size", "pa_decode", "pa_prefill_workspace_size", "pa_prefill_chunk",
-           "pa_copy_blocks")
+           "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_prefill_workspace_size",
+           "pa_prefill_chunk", "pa_copy_blocks")
 
 
 class PaError(RuntimeError):
@@ -42,6 +42,7 @@ _SIGNATURES = {
     "pa_write_kv": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _p, _p], _i),
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
+    "pa_decode_noalloc": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p], _i),
     "pa_prefill_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_prefill_chunk": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _f, _p,
                           _sz, _p, _p], _i),
@@ -160,6 +161,26 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return out
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                      out=None, error_count=None, stream=None) -> torch.Tensor:
+    """pa_decode without a workspace argument, for callers that cannot allocate
+    device memory: the split-KV scratch is the library's own fixed 16 MiB device
+    array.  Sizes that need more scratch raise PaError (PA_ERR_WORKSPACE).
+    Calls that may overlap on the GPU share that array and race."""
+    N, Hq, D = q.shape
+    P, B, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_cache differ")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode_noalloc", lib().pa_decode_noalloc(
+        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
     return out
 
