@@ -9,11 +9,15 @@ bf16, random non-contiguous block tables.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints ONE JSON line (rank 0).  ``value`` is decode tokens/s (one token per
-sequence per step) over all ranks; the roofline object describes the decode
-kernel (algorithmic K/V bytes per launch / its CUDA-event time, against the
-measured HBM copy bandwidth).  L2 is flushed (a 512 MiB write) before every
-timed step.  Under torchrun each rank runs an independent replica with its
-own seed (weak scaling, no collective on the data path).
+sequence per step) over all ranks, timed over exactly K steps, each a replay
+of the step captured as a CUDA graph (``--no-graph``: eager launches).  The
+roofline object describes the decode kernel (algorithmic K/V bytes per launch
+/ its CUDA-event time over eager launches, against the measured HBM copy
+bandwidth).  ``e2e`` re-times the step eagerly through the public API with
+pinned-host inputs copied in and the outputs copied out inside the events.
+L2 is flushed (a 512 MiB write) before every timed step.  Under torchrun each
+rank runs an independent shard with its own seed (weak scaling, no collective
+on the data path).
 """
 from __future__ import annotations
 
@@ -48,6 +52,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch the timed steps eagerly instead of replaying a captured CUDA graph")
     return ap.parse_args()
 
 
@@ -277,9 +283,16 @@ def run_native(args):
         flush.fill_(1)
         step.run()
     barrier()
+    if args.graph:
+        step.capture()
+        for _ in range(3):
+            flush.fill_(1)
+            step.replay()
+        barrier()
 
+    # ---- timed region: exactly K whole steps, L2 flushed before each (outside the events)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = visible.split(",")[local].strip() if visible else str(local)
     sampler = ClockSampler(smi_index)
@@ -287,7 +300,22 @@ def run_native(args):
     barrier()
     t0 = time.time()
     for i in range(K):
-        e = ev[i]
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        if args.graph:
+            step.replay()
+        else:
+            step.run()
+        ev[i][1].record(stream)
+    barrier()
+    t1 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- per-kernel times (eager launches, same flush) for the roofline
+    K1 = max(3, min(K, 100))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K1)]
+    for i in range(K1):
+        e = kev[i]
         flush.fill_(i & 0xFF)
         e[0].record(stream)
         step.slot_mapping()
@@ -298,13 +326,11 @@ def run_native(args):
         step.prefill()
         e[3].record(stream)
     barrier()
-    t1 = time.time()
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    prefill_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    write_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    decode_ms = [e[1].elapsed_time(e[2]) for e in kev]
+    prefill_ms = [e[2].elapsed_time(e[3]) for e in kev]
 
-    # end to end through the public API: pinned host inputs -> device, step, output -> host
+    # ---- end to end through the public API: pinned host inputs -> device, step, output -> host
     host_in = [t.detach().cpu().pin_memory() for t in step_input_tensors(step)]
     host_out_d = torch.empty(step.out_decode.shape, dtype=step.out_decode.dtype).pin_memory()
     host_out_p = torch.empty(step.out_prefill.shape, dtype=step.out_prefill.dtype).pin_memory()
@@ -349,7 +375,8 @@ def run_native(args):
         "stage_ms": {"slot_mapping+write_kv": statistics.mean(write_ms), "decode": mean_dec,
                      "prefill": statistics.mean(prefill_ms)},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2},
+                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2, "launch": "eager"},
+        "step_launch": "cuda_graph" if args.graph else "eager",
         "gpu_launches": K * launches_per_step,
         "clocks": sampler.summary(t0, t1),
         "device_errors": errors,

@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(DecodeParams p)
     using S = FmaShape<D>;
     const int s = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
     const int G = p.group;
-    const int L = decode_context(p, s, split);
+    const int L = decode_context(p, s, split == 0 && threadIdx.x == 0);
     const int nsplit = num_partitions(L, p.partition);
     if (split >= nsplit) return;
     const int j0 = split * p.partition;

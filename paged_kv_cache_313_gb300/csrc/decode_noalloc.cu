@@ -84,6 +84,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     p.context_lens = context_lens;
     p.error_count = error_count;
     p.counters = reinterpret_cast<int*>(ws + lay.counters);
+    p.work = p.counters + (size_t)num_seqs * num_kv_heads;
     p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
     p.ws_o = reinterpret_cast<float*>(ws + lay.o);
     p.num_seqs = num_seqs;
@@ -98,6 +99,6 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     p.partition = plan.partition;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, st);
+    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, num_sms, st);
     return launch_decode_fma(p, dtype, st);
 }

@@ -90,7 +90,7 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
     size_t units = (size_t)num_seqs * num_kv_heads;
     size_t group = (size_t)(num_q_heads / num_kv_heads);
     w.counters = 0;
-    w.ml = align_up(units * sizeof(int), 256);
+    w.ml = align_up((units + 2) * sizeof(int), 256);
     w.o = align_up(w.ml + units * max_splits * group * sizeof(float2), 256);
     w.total = align_up(w.o + units * max_splits * group * head_dim * sizeof(float), 256);
     return w;
@@ -215,6 +215,7 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
     p.context_lens = context_lens;
     p.error_count = error_count;
     p.counters = reinterpret_cast<int*>(ws + lay.counters);
+    p.work = p.counters + (size_t)num_seqs * num_kv_heads;
     p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
     p.ws_o = reinterpret_cast<float*>(ws + lay.o);
     p.num_seqs = num_seqs;
@@ -229,7 +230,7 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
     p.partition = plan.partition;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, static_cast<cudaStream_t>(stream));
+    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, num_sms, static_cast<cudaStream_t>(stream));
     return launch_decode_fma(p, dtype, static_cast<cudaStream_t>(stream));
 }
 
@@ -279,6 +280,7 @@ int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const i
     p.block_size = block_size;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.scale_log2 = scale * 1.4426950408889634f;
+    if (prefill_tc_supported(p, dtype)) return launch_prefill_tc(p, static_cast<cudaStream_t>(stream));
     return launch_prefill_fma(p, dtype, static_cast<cudaStream_t>(stream));
 }
 

@@ -30,7 +30,7 @@ DecodePlan plan_decode(int num_seqs, int num_kv_heads, int max_context_len, int 
 
 // Workspace layout of pa_decode (byte offsets from the 256-aligned base).
 struct DecodeWorkspace {
-    size_t counters;  // int32 [num_seqs][num_kv_heads]
+    size_t counters;  // int32 [num_seqs][num_kv_heads] tickets, then 2 work-queue counters
     size_t ml;        // float2 [num_seqs][num_kv_heads][max_splits][G]  (running max in log2 units, sum)
     size_t o;         // float  [num_seqs][num_kv_heads][max_splits][G][head_dim]
     size_t total;
@@ -46,7 +46,8 @@ struct DecodeParams {
     const int32_t* block_tables;
     const int32_t* context_lens;
     int32_t* error_count;
-    int* counters;
+    int* counters;      // ticket per (sequence, kv head)
+    int* work;          // work[0]: next item, work[1]: finished CTAs (persistent kernel)
     float2* ws_ml;
     float* ws_o;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
@@ -85,7 +86,9 @@ int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_s
                        int32_t* error_count, cudaStream_t stream);
 int launch_decode_fma(const DecodeParams& p, int dtype, cudaStream_t stream);
 bool decode_tc_supported(const DecodeParams& p, int dtype);
-int launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream);
+bool prefill_tc_supported(const PrefillParams& p, int dtype);
+int launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- device side
 __device__ __forceinline__ float to_float(float x) { return x; }

@@ -1,0 +1,425 @@
+// prefill_tc.cu — causal chunked prefill over the paged pool on the 5th-gen
+// tensor cores (tcgen05, accumulators in TMEM), bf16.
+//
+// What it computes ("什么是 PagedAttention？", 工作原理: prefill takes blocks for
+// the input length; "KV cache 显存管理…", PagedAttention 改变了什么: keys are
+// found through the block table): query i of chunk c, at absolute position
+// p = q_start_pos[c] + i, attends keys 0..p of its sequence, the chunk's own
+// keys included (they were written to the pool first).
+//
+// One CTA per (128-row query tile, kv head, chunk).  The G query heads that
+// share a kv head are packed into the tile's rows: row r is position
+// i0 + r/G, head r%G, so every K/V tile is loaded once for all G heads.
+// Key tiles are 128 keys, gathered block by block from the pool by TMA
+// (one box per physical block and 64-column half, 128-byte swizzled).
+//
+// Warp roles (192 threads):
+//   warp 0    TMA producer: the Q tile once, then K and V tiles into two
+//             2-deep rings; K and V are released separately (K after its
+//             QK^T MMA, V after its PV MMA) so the next K streams early.
+//   warp 1    TMEM owner and MMA issuer (one thread):
+//               S_j = Q K_j^T      M=128 N=128 K=128   -> TMEM S[j%2]
+//               O  += P_j V_j      M=128 N=128 K=128   -> TMEM O
+//             S is double-buffered, so QK^T of tile j+1 runs on the tensor
+//             cores while the softmax warps work on tile j.
+//   warps 2-5 softmax, one query row per thread (TMEM lane = row): read S,
+//             mask (causal and context), online softmax in base-2 units with
+//             a lazy rescale (O in TMEM is rescaled only when the row max
+//             grows by more than 2^8), write P as bf16 into a swizzled shared
+//             tile for the PV MMA, zero V rows past the last valid key, and
+//             finally normalise O and store the output rows.
+// All waits are bounded (an error is counted and the kernel still finishes);
+// TMEM is always freed.
+#include "pa_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTileQ = 128;      // query rows per tile
+constexpr int kTileK = 128;      // keys per tile
+constexpr int kD = 128;          // head_dim handled by this kernel
+constexpr int kHalf = 128 * 128; // bytes of one 64-column half of a 128-row tile
+constexpr int kTileBytes = 2 * kHalf;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | unused
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+
+struct VInfo {
+    uint32_t valid[4];  // bit k of word k/32: key k of the tile holds a valid token
+};
+
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kQ = 0;
+constexpr int kK = kQ + kTileBytes;      // 2 stages
+constexpr int kV = kK + 2 * kTileBytes;  // 2 stages
+constexpr int kP = kV + 2 * kTileBytes;
+constexpr int kInfo = kP + kTileBytes;   // VInfo[2]
+constexpr int kBars = kInfo + 2 * (int)sizeof(VInfo);
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, o_done
+constexpr int kNumBars = 1 + 2 * 6 + 2;
+constexpr int kTmemSlot = kBars + kNumBars * 8;
+constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
+
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+struct Bars {
+    uint64_t* base;
+    __device__ uint64_t* q_full() const { return base; }
+    __device__ uint64_t* k_full(int i) const { return base + 1 + i; }
+    __device__ uint64_t* k_empty(int i) const { return base + 3 + i; }
+    __device__ uint64_t* v_full(int i) const { return base + 5 + i; }
+    __device__ uint64_t* v_empty(int i) const { return base + 7 + i; }
+    __device__ uint64_t* s_full(int i) const { return base + 9 + i; }
+    __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
+    __device__ uint64_t* p_full() const { return base + 13; }
+    __device__ uint64_t* o_done() const { return base + 14; }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+    const int c = blockIdx.z, kvh = blockIdx.y;
+    const int G = p.group, B = p.block_size;
+    const int pos_per_tile = kTileQ / G;
+
+    // ---- chunk descriptor (every thread, identical)
+    const int r0 = p.cu_q_lens[c];
+    const int n = p.cu_q_lens[c + 1] - r0;
+    const int s = p.seq_of_chunk[c];
+    const int start = p.q_start_pos[c];
+    const bool chunk_ok = n >= 0 && r0 >= 0 && r0 + n <= p.total_q && n <= p.max_q_len && s >= 0 &&
+                          s < p.num_seqs && start >= 0;
+    if (!chunk_ok) {
+        if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) count_error(p.error_count);
+        return;
+    }
+    const int ntiles_q = (n + pos_per_tile - 1) / pos_per_tile;
+    if ((int)blockIdx.x >= ntiles_q) return;
+    const int tile = ntiles_q - 1 - blockIdx.x;  // heaviest (latest) tiles first
+    const int i0 = tile * pos_per_tile;
+    const int nq = min(pos_per_tile, n - i0);
+    const int cap = min(p.context_lens[s], p.max_blocks_per_seq * B);
+    int last_key = start + i0 + nq - 1;  // the tile's last query position
+    if (last_key >= cap) {
+        if (threadIdx.x == 0) count_error(p.error_count);
+        last_key = cap - 1;
+    }
+    const int nkeys = last_key + 1;  // keys 0..last_key are read
+    const int nt = nkeys > 0 ? (nkeys + kTileK - 1) / kTileK : 0;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Bars bars{reinterpret_cast<uint64_t*>(smem + kBars)};
+    VInfo* vinfo = reinterpret_cast<VInfo*>(smem + kInfo);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars.q_full(), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.k_full(i), 1);
+            mbar_init(bars.k_empty(i), 1);
+            mbar_init(bars.v_full(i), 1);
+            mbar_init(bars.v_empty(i), 1);
+            mbar_init(bars.s_full(i), 1);
+            mbar_init(bars.s_empty(i), 4);
+        }
+        mbar_init(bars.p_full(), 4);
+        mbar_init(bars.o_done(), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ============================================================ producer
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        const int nblk = (nkeys + B - 1) / B;
+        const int bpt = kTileK / B;  // blocks per key tile
+        if (lane == 0 && nt > 0) {  // with no keys nothing is loaded (and nothing may be left in flight)
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            mbar_arrive_expect_tx(bars.q_full(), 2 * kHalf);
+            for (int h = 0; h < 2; ++h)
+                tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, r0 + i0, bars.q_full());
+        }
+        int chunk = -1, pb_lane = -1;
+        for (int j = 0; j < nt; ++j) {
+            const int st = j & 1;
+            const int b0 = j * bpt;
+            if ((b0 >> 5) != chunk) {  // a tile's blocks never straddle a 32-entry chunk
+                chunk = b0 >> 5;
+                const int idx = chunk * 32 + lane;
+                pb_lane = -1;
+                if (idx < nblk) {
+                    pb_lane = table[idx];
+                    if (pb_lane < 0 || pb_lane >= p.num_blocks) {
+                        count_error(p.error_count);
+                        pb_lane = -1;
+                    }
+                }
+            }
+            uint32_t vmask[4] = {0u, 0u, 0u, 0u};
+            uint32_t bytes = 0;
+            for (int b = 0; b < bpt; ++b) {
+                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
+                if (b0 + b < nblk && pb >= 0) {
+                    bytes += 2u * B * 128u;
+                    for (int k = b * B; k < (b + 1) * B; ++k)
+                        if (j * kTileK + k < nkeys) vmask[k >> 5] |= 1u << (k & 31);
+                }
+            }
+            // K tile j
+            if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(bars.k_full(st), bytes);
+            for (int b = 0; b < bpt; ++b) {
+                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
+                if (lane == 0 && b0 + b < nblk && pb >= 0)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + b * B * 128, &tmk, kvh * kD + h * 64,
+                                    pb * B, bars.k_full(st));
+            }
+            // V tile j, with the validity of its keys
+            if (j >= 2 && !mbar_wait(bars.v_empty(st), ((j - 2) >> 1) & 1)) ok = false;
+            if (!ok) break;
+            if (lane == 0) {
+                for (int w = 0; w < 4; ++w) vinfo[st].valid[w] = vmask[w];
+                mbar_arrive_expect_tx(bars.v_full(st), bytes);
+            }
+            for (int b = 0; b < bpt; ++b) {
+                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
+                if (lane == 0 && b0 + b < nblk && pb >= 0)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(smem + kV + st * kTileBytes + h * kHalf + b * B * 128, &tmv, kvh * kD + h * 64,
+                                    pb * B, bars.v_full(st));
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0) count_error(p.error_count);
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
+            const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
+            const uint32_t v_base = smem_u32(smem + kV), p_base = smem_u32(smem + kP);
+            const uint32_t t_o = tmem + 256;
+            if (nt > 0 && !mbar_wait(bars.q_full(), 0)) ok = false;
+            for (int j = 0; j <= nt && ok; ++j) {
+                if (j < nt) {  // S_j = Q K_j^T into S[j%2]
+                    const int st = j & 1;
+                    if (!mbar_wait(bars.k_full(st), (j >> 1) & 1)) { ok = false; break; }
+                    if (j >= 2 && !mbar_wait(bars.s_empty(st), ((j - 2) >> 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kb = k_base + st * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        umma_bf16(tmem + st * 128, umma_desc_sw128(q_base + off, 16, 1024),
+                                  umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                    }
+                    umma_commit(bars.s_full(st));
+                    umma_commit(bars.k_empty(st));
+                }
+                if (j >= 1) {  // O += P_{j-1} V_{j-1}
+                    const int jj = j - 1, st = jj & 1;
+                    if (!mbar_wait(bars.p_full(), jj & 1)) { ok = false; break; }
+                    if (!mbar_wait(bars.v_full(st), (jj >> 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t vb = v_base + st * kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        umma_bf16(t_o, umma_desc_sw128(p_base + poff, 16, 1024),
+                                  umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, jj > 0 || kk > 0);
+                    }
+                    umma_commit(bars.o_done());
+                    umma_commit(bars.v_empty(st));
+                }
+            }
+            if (!ok) count_error(p.error_count);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ softmax / epilogue
+        const int quarter = warp & 3;       // TMEM lane quarter this warp may access
+        const int r = quarter * 32 + lane;  // the query row this thread owns
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int pos = i0 + r / G;  // chunk-relative position
+        const bool row_ok = pos - i0 < nq;
+        const int my_last = min(start + pos, last_key);  // last key this row may see
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        uint8_t* p_tile = smem + kP;
+        for (int j = 0; j < nt && ok; ++j) {
+            const int st = j & 1;
+            if (!mbar_wait(bars.s_full(st), (j >> 1) & 1)) { ok = false; break; }
+            if (!mbar_wait(bars.v_full(st), (j >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            float sv[kTileK];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float t[32];
+                tmem_ld32(tmem + lane_off + st * 128 + q4 * 32, t);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sv[q4 * 32 + i] = t[i];
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_empty(st));
+            const uint32_t vm[4] = {vinfo[st].valid[0], vinfo[st].valid[1], vinfo[st].valid[2], vinfo[st].valid[3]};
+            const int kbase = j * kTileK;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kTileK; ++k) {
+                const bool valid = ((vm[k >> 5] >> (k & 31)) & 1u) && kbase + k <= my_last;
+                sv[k] = valid ? sv[k] * sl2 : -INFINITY;
+                mt = fmaxf(mt, sv[k]);
+            }
+            // PV_{j-1} must be complete before O is rescaled or P overwritten
+            if (j > 0 && !mbar_wait(bars.o_done(), (j - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
+                if (m_run != -INFINITY) {
+                    const float alpha = exp2f(m_run - mt);
+                    l_run *= alpha;
+                    if (j > 0) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float t[32];
+                            tmem_ld32(tmem + lane_off + 256 + q4 * 32, t);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) t[i] *= alpha;
+                            tmem_st32(tmem + lane_off + 256 + q4 * 32, t);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                m_run = mt;
+            }
+            // P = 2^(x - m) in bf16, written to the swizzled shared tile (row r)
+            float lsum = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < kTileK / 8; ++ch) {
+                float e[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float x = sv[ch * 8 + i];
+                    e[i] = (x == -INFINITY) ? 0.f : exp2f(x - m_run);
+                    lsum += e[i];
+                }
+                uint4 pk;
+                pk.x = pack_bf16x2(e[0], e[1]);
+                pk.y = pack_bf16x2(e[2], e[3]);
+                pk.z = pack_bf16x2(e[4], e[5]);
+                pk.w = pack_bf16x2(e[6], e[7]);
+                *reinterpret_cast<uint4*>(p_tile + (ch >> 3) * kHalf + swz(r, ch & 7)) = pk;
+            }
+            l_run += lsum;
+            // V row r carries no valid key for any row: zero it (stale or non-finite pool bytes)
+            if (!((vm[r >> 5] >> (r & 31)) & 1u)) {
+                uint8_t* vrow = smem + kV + st * kTileBytes;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4*>(vrow + h * kHalf + r * 128 + c8 * 16) = z;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full());
+        }
+        // ---- epilogue: O / l -> out
+        if (ok && nt > 0 && !mbar_wait(bars.o_done(), (nt - 1) & 1)) ok = false;
+        tc_fence_after();
+        if (!ok && lane == 0) count_error(p.error_count);
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
+                             ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float t[32];
+            if (nt > 0) {
+                tmem_ld32(tmem + lane_off + 256 + q4 * 32, t);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = 0.f;
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(t[i] * inv, t[i + 1] * inv);
+                    pk.y = pack_bf16x2(t[i + 2] * inv, t[i + 3] * inv);
+                    pk.z = pack_bf16x2(t[i + 4] * inv, t[i + 5] * inv);
+                    pk.w = pack_bf16x2(t[i + 6] * inv, t[i + 7] * inv);
+                    *reinterpret_cast<uint4*>(out + q4 * 32 + i) = pk;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillParams& p, int dtype) {
+    const int G = p.group, B = p.block_size;
+    if (dtype != PA_BF16 || p.head_dim != kD) return false;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+    if (B != 8 && B != 16 && B != 32 && B != 64 && B != 128) return false;
+    if (((uintptr_t)p.q & 15) || ((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) ||
+        ((uintptr_t)p.out & 15))
+        return false;
+    if ((long long)p.num_blocks * B >= (1LL << 31)) return false;
+    return p.num_chunks <= 65535 && p.num_kv_heads <= 65535;
+}
+
+int launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
+    CUtensorMap tmq, tmk, tmv;
+    {
+        auto enc = tensor_map_encoder();
+        if (!enc) return PA_ERR_CUDA;
+        const int G = p.group;
+        // q as [total_q][Hq][D]: a box is 128/G positions x the G heads of one kv head x 64 columns
+        cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.num_q_heads, (cuuint64_t)p.total_q};
+        cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.num_q_heads * kD * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kTileQ / G)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = enc(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.q), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return PA_ERR_UNSUPPORTED;
+    }
+    int rc = pool_tensor_map(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, kD);
+    if (rc != PA_OK) return rc;
+    if ((rc = pool_tensor_map(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, kD)) != PA_OK) return rc;
+    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_tc_kernel), kSmemBytes)) != PA_OK) return rc;
+    const int pos_per_tile = kTileQ / p.group;
+    dim3 grid((p.max_q_len + pos_per_tile - 1) / pos_per_tile, p.num_kv_heads, p.num_chunks);
+    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmq, tmk, tmv, p);
+    return check_launch();
+}
+
+}  // namespace pa

@@ -80,5 +80,25 @@ class DeviceStep:
         self.prefill(stream)
         return self.out_decode, self.out_prefill
 
+    def capture(self) -> "torch.cuda.CUDAGraph":
+        """Record one whole step (the four library calls) as a CUDA graph, so a
+        serving loop replays it with one launch.  Call after at least one eager
+        step (first calls configure the kernels)."""
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        """Replay the captured step on the current stream."""
+        self.graph.replay()
+        return self.out_decode, self.out_prefill
+
     def errors(self) -> int:
         return int(self.error_count.item()) if self.error_count is not None else 0

@@ -227,6 +227,31 @@ def mixed_bf16(seed: int = 0, num_decode: int = 256, num_chunks: int = 4, chunk_
                    chunk_seqs=cseqs, chunk_off=[int(o) for o in offs], chunk_len=[chunk_len] * num_chunks)
 
 
+def prefill_batch(seed: int, num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int, chunk_lens,
+                  offsets, dtype: torch.dtype = torch.bfloat16, decode_lens=()) -> Workload:
+    """A batch of chunked-prefill requests (chunk c: ``chunk_lens[c]`` queries at
+    prior offset ``offsets[c]``), optionally with decode sequences, for any head
+    layout and block size."""
+    B = block_size
+    needed = sum(-(-int(L) // B) for L in decode_lens) + sum(-(-(int(o) + int(n)) // B)
+                                                          for o, n in zip(offsets, chunk_lens))
+    alloc = BlockAllocator(_pool_size(max(needed, 1)) + 4, B, seed=seed + 1)
+    dseqs = []
+    for L in decode_lens:
+        s = alloc.allocate(int(L) - 1)
+        alloc.append(s, 1)
+        dseqs.append(s)
+    cseqs = []
+    for o, n in zip(offsets, chunk_lens):
+        s = alloc.allocate(int(o))
+        alloc.append(s, int(n))
+        cseqs.append(s)
+    vrng = np.random.default_rng(seed)
+    return _finish(f"prefill_g{num_q_heads // num_kv_heads}_b{B}", dtype, num_q_heads, num_kv_heads, head_dim, B,
+                   alloc, vrng, dseqs, [int(L) for L in decode_lens], chunk_seqs=cseqs,
+                   chunk_off=[int(o) for o in offsets], chunk_len=[int(n) for n in chunk_lens])
+
+
 def small(name: str, seed: int = 0) -> Workload:
     """Reduced-size versions of the bf16 workloads (same shapes per token, fewer and
     shorter sequences) for quick parity runs that still span several tiles and

@@ -199,3 +199,42 @@ def test_shared_prefix_branches_identical_after_device_cow():
     q = torch.randn(1, Hq, D, generator=g).to(torch.bfloat16).cuda().repeat(2, 1, 1)
     out = _decode_direct(q, kc, vc, bt, i32([2051, 2051]), 2051, 1 / math.sqrt(D))
     assert torch.equal(out[0], out[1])
+
+
+PREFILL_CASES = [
+    # (Hq, Hkv, B, chunk_lens, offsets, dtype)
+    (32, 8, 32, [512, 200], [0, 700], torch.bfloat16),
+    (64, 8, 16, [129, 1, 33], [5, 0, 1000], torch.bfloat16),
+    (8, 8, 64, [300], [64], torch.bfloat16),
+    (16, 8, 128, [77, 256], [130, 0], torch.bfloat16),
+    (32, 8, 8, [96], [1500], torch.bfloat16),
+    (8, 4, 16, [70, 9], [3, 40], torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
+def test_prefill_shapes(case):
+    Hq, Hkv, B, lens, offs, dt = PREFILL_CASES[case]
+    w = W.prefill_batch(100 + case, Hq, Hkv, 128, B, lens, offs, dtype=dt, decode_lens=[1, 37])
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    err = _maxabs(st.out_prefill, exp.out_prefill)
+    assert err <= TOL[dt], f"prefill max-abs error {err}"
+    assert _maxabs(st.out_decode, exp.out_decode) <= TOL[dt]
+    assert st.errors() == 0
+
+
+def test_graph_replay_matches_eager():
+    """The captured step (CUDA graph of the four library calls) gives the same
+    outputs as eager calls, replay after replay."""
+    w, _ = _case("small", "mixed_bf16")
+    st = DeviceStep(w)
+    want = [t.clone() for t in st.run()]
+    st.capture()
+    for _ in range(3):
+        got = st.replay()
+        torch.cuda.synchronize()
+        for x, y in zip(want, got):
+            assert torch.equal(x, y)
