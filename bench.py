@@ -174,6 +174,19 @@ def prefill_flops(w) -> float:
     return 4.0 * w.head_dim * w.num_q_heads * tot
 
 
+def kv_memory(w):
+    """Per-request KV footprint and fragmentation of the workload's block tables
+    next to a contiguous max-length reservation (host-side measurement)."""
+    from paged_kv_cache_313_gb300.memstats import utilisation
+
+    if w.allocator is None:
+        return None
+    u = utilisation(w.allocator, w.seq_ids, w.kv_bytes_per_token())
+    keep = ("per_request_bytes_mean", "per_request_bytes_p95", "pool_bytes_used", "fragmentation",
+            "max_tail_waste_slots", "contiguous_reserved_bytes", "contiguous_waste")
+    return {k: u[k] for k in keep}
+
+
 def step_input_tensors(step):
     """The per-step inputs a serving loop hands to the path (the pools are resident state)."""
     return [step.q_decode, step.k_new, step.v_new, step.block_tables, step.context_lens, step.seq_idx, step.pos,
@@ -378,6 +391,7 @@ def run_native(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2, "launch": "eager"},
         "step_launch": "cuda_graph" if args.graph else "eager",
         "gpu_launches": K * launches_per_step,
+        "kv_memory": kv_memory(w),
         "clocks": sampler.summary(t0, t1),
         "device_errors": errors,
     }

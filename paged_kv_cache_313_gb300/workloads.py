@@ -55,6 +55,8 @@ class Workload:
     q_prefill: torch.Tensor  # [total_q, Hq, D]
     cow_copies: list = field(default_factory=list)
     meta: dict = field(default_factory=dict)
+    allocator: BlockAllocator | None = None  # the allocator state that produced the tables
+    seq_ids: list = field(default_factory=list)  # allocator ids of the table's rows
 
     @property
     def num_seqs(self) -> int:
@@ -125,7 +127,7 @@ def _finish(name, dtype, Hq, Hkv, D, B, alloc: BlockAllocator, rng, decode_seqs,
         cu_q_lens=torch.tensor(cu, dtype=torch.int32),
         q_start_pos=torch.tensor(list(chunk_off), dtype=torch.int32),
         seq_of_chunk=torch.tensor([nd + i for i in range(len(chunk_off))], dtype=torch.int32),
-        q_prefill=q_prefill, cow_copies=list(cow), meta=dict(meta or {}))
+        q_prefill=q_prefill, cow_copies=list(cow), meta=dict(meta or {}), allocator=alloc, seq_ids=seqs)
 
 
 def _pool_size(needed_blocks: int, spare: float = 0.10) -> int:
