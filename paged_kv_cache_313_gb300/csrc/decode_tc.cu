@@ -46,7 +46,14 @@
 namespace pa {
 namespace {
 
-constexpr int kMaxSeqsPersistent = 2048;
+// Ring depth and CTAs per SM (build-time knobs; the defaults are the measured best).
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 5
+#endif
+#ifndef PA_DECODE_CTAS_PER_SM
+#define PA_DECODE_CTAS_PER_SM 1
+#endif
+constexpr int kMaxSeqsPersistent = PA_DECODE_CTAS_PER_SM == 1 ? 2048 : 1024;
 
 struct StageInfo {
     int s, kvh, split, nsplit;
@@ -59,7 +66,7 @@ template <int D>
 struct TcCfg {
     static constexpr int kHalves = D / 64;               // 64-column (128-byte) halves of a row
     static constexpr int kStageTok = 64;
-    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kStages = D == 128 ? PA_DECODE_STAGES : 2 * PA_DECODE_STAGES;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kHalfBytes = kStageTok * 128;   // one half of a stage's K (or V) tile
@@ -76,7 +83,7 @@ struct TcCfg {
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
     static constexpr int kEnd = kBars + 2 * kStages * 8;
     static constexpr size_t kSmemBytes = 1024 + kEnd;
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kSmemBytes * PA_DECODE_CTAS_PER_SM <= 227 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -102,7 +109,7 @@ __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int 
 }
 
 template <int D>
-__global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeParams p, int* work) {
     using C = TcCfg<D>;
@@ -237,17 +244,17 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                                       ((size_t)s * p.num_q_heads + (size_t)kvh * G) * D,
                                   (uint32_t)(G * D * 2), &full[slot]);
                 }
+                __syncwarp();  // the transaction count is armed before any copy is issued
+                // one lane per block issues that block's copies, so the stage's boxes go out together
                 uint8_t* kdst = smem + C::kRing + slot * C::kStageBytes;
                 uint8_t* vdst = kdst + C::kTileBytes;
-                for (int b = 0; b < nb; ++b) {
-                    const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                    if (lane == 0 && pb >= 0) {
+                const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
+                if (lane < nb && my_pb >= 0) {
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h) {
-                            const int x = kvh * D + h * 64;
-                            tma_load_2d(kdst + h * C::kHalfBytes + b * B * 128, &tmk, x, pb * B, &full[slot]);
-                            tma_load_2d(vdst + h * C::kHalfBytes + b * B * 128, &tmv, x, pb * B, &full[slot]);
-                        }
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        const int x = kvh * D + h * 64;
+                        tma_load_2d(kdst + h * C::kHalfBytes + lane * B * 128, &tmk, x, my_pb * B, &full[slot]);
+                        tma_load_2d(vdst + h * C::kHalfBytes + lane * B * 128, &tmv, x, my_pb * B, &full[slot]);
                     }
                 }
                 __syncwarp();
@@ -348,12 +355,12 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
                 }
                 const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-                const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-                const float p0 = mn0 == -INFINITY ? 0.f : exp2f(x0 - mn0);
-                const float p2 = mn0 == -INFINITY ? 0.f : exp2f(x2 - mn0);
-                const float p1 = mn1 == -INFINITY ? 0.f : exp2f(x1 - mn1);
-                const float p3 = mn1 == -INFINITY ? 0.f : exp2f(x3 - mn1);
+                const float a0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
+                const float a1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
+                const float p0 = mn0 == -INFINITY ? 0.f : fast_exp2(x0 - mn0);
+                const float p2 = mn0 == -INFINITY ? 0.f : fast_exp2(x2 - mn0);
+                const float p1 = mn1 == -INFINITY ? 0.f : fast_exp2(x1 - mn1);
+                const float p3 = mn1 == -INFINITY ? 0.f : fast_exp2(x3 - mn1);
                 l0 = l0 * a0 + p0 + p2;
                 l1 = l1 * a1 + p1 + p3;
                 m0 = mn0;
@@ -405,8 +412,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 M0 = fmaxf(M0, red_m[w][2 * c4]);
                 M1 = fmaxf(M1, red_m[w][2 * c4 + 1]);
             }
-            const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-            const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+            const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
+            const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
             float* ored = reinterpret_cast<float*>(smem + C::kOred);
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
 #pragma unroll
                 for (int w = 0; w < C::kConsumerWarps; ++w) {
                     const float mw = red_m[w][h];
-                    if (mw != -INFINITY) Ls += red_l[w][h] * exp2f(mw - M);
+                    if (mw != -INFINITY) Ls += red_l[w][h] * fast_exp2(mw - M);
                     acc += ored[(w * 8 + h) * D + d];
                 }
                 const float val = Ls > 0.f ? acc / Ls : 0.f;
@@ -470,9 +477,10 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     if ((rc = pool_tensor_map(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D)) != PA_OK) return rc;
     if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D>), C::kSmemBytes)) != PA_OK)
         return rc;
-    // at most one CTA per SM, never more CTAs than the largest possible item count
+    // PA_DECODE_CTAS_PER_SM CTAs per SM, never more CTAs than the largest possible item count
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
-    int grid = (int)(max_items < num_sms ? max_items : num_sms);
+    const long long slots = (long long)num_sms * PA_DECODE_CTAS_PER_SM;
+    int grid = (int)(max_items < slots ? max_items : slots);
     decode_tc_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmk, tmv, p, p.work);
     return check_launch();
 }

@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
             if (!ok) break;
             if (lane == 0) mbar_arrive_expect_tx(bars.k_full(st), bytes);
-            for (int b = 0; b < bpt; ++b) {
-                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                if (lane == 0 && b0 + b < nblk && pb >= 0)
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + b * B * 128, &tmk, kvh * kD + h * 64,
-                                    pb * B, bars.k_full(st));
-            }
+            __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
+            const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
+            const bool my_load = lane < bpt && b0 + lane < nblk && my_pb >= 0;
+            if (my_load)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + lane * B * 128, &tmk, kvh * kD + h * 64,
+                                my_pb * B, bars.k_full(st));
             // V tile j, with the validity of its keys
             if (j >= 2 && !mbar_wait(bars.v_empty(st), ((j - 2) >> 1) & 1)) ok = false;
             if (!ok) break;
@@ -198,13 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int w = 0; w < 4; ++w) vinfo[st].valid[w] = vmask[w];
                 mbar_arrive_expect_tx(bars.v_full(st), bytes);
             }
-            for (int b = 0; b < bpt; ++b) {
-                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                if (lane == 0 && b0 + b < nblk && pb >= 0)
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(smem + kV + st * kTileBytes + h * kHalf + b * B * 128, &tmv, kvh * kD + h * 64,
-                                    pb * B, bars.v_full(st));
-            }
+            __syncwarp();
+            if (my_load)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(smem + kV + st * kTileBytes + h * kHalf + lane * B * 128, &tmv, kvh * kD + h * 64,
+                                my_pb * B, bars.v_full(st));
             __syncwarp();
         }
         if (!ok && lane == 0) count_error(p.error_count);
@@ -294,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
                 if (m_run != -INFINITY) {
-                    const float alpha = exp2f(m_run - mt);
+                    const float alpha = fast_exp2(m_run - mt);
                     l_run *= alpha;
                     if (j > 0) {
 #pragma unroll
@@ -319,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float x = sv[ch * 8 + i];
-                    e[i] = (x == -INFINITY) ? 0.f : exp2f(x - m_run);
+                    e[i] = (x == -INFINITY) ? 0.f : fast_exp2(x - m_run);
                     lsum += e[i];
                 }
                 uint4 pk;
