@@ -48,10 +48,10 @@ namespace {
 
 // Ring depth and CTAs per SM (build-time knobs; the defaults are the measured best).
 #ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 5
+#define PA_DECODE_STAGES 2
 #endif
 #ifndef PA_DECODE_CTAS_PER_SM
-#define PA_DECODE_CTAS_PER_SM 1
+#define PA_DECODE_CTAS_PER_SM 2
 #endif
 constexpr int kMaxSeqsPersistent = PA_DECODE_CTAS_PER_SM == 1 ? 2048 : 1024;
 

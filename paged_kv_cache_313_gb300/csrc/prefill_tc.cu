@@ -14,9 +14,9 @@
 // (one box per physical block and 64-column half, 128-byte swizzled).
 //
 // Warp roles (192 threads):
-//   warp 0    TMA producer: the Q tile once, then K and V tiles into two
-//             2-deep rings; K and V are released separately (K after its
-//             QK^T MMA, V after its PV MMA) so the next K streams early.
+//   warp 0    TMA producer: the Q tile once, then K tiles into a 2-deep and
+//             V tiles into a 3-deep ring; K and V are released separately (K
+//             after its QK^T MMA, V after its PV MMA) so loads run ahead.
 //   warp 1    TMEM owner and MMA issuer (one thread):
 //               S_j = Q K_j^T      M=128 N=128 K=128   -> TMEM S[j%2]
 //               O  += P_j V_j      M=128 N=128 K=128   -> TMEM O
@@ -45,19 +45,15 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | unused
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
-struct VInfo {
-    uint32_t valid[4];  // bit k of word k/32: key k of the tile holds a valid token
-};
-
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kQ = 0;
 constexpr int kK = kQ + kTileBytes;      // 2 stages
-constexpr int kV = kK + 2 * kTileBytes;  // 2 stages
-constexpr int kP = kV + 2 * kTileBytes;
-constexpr int kInfo = kP + kTileBytes;   // VInfo[2]
-constexpr int kBars = kInfo + 2 * (int)sizeof(VInfo);
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, o_done
-constexpr int kNumBars = 1 + 2 * 6 + 2;
+constexpr int kVStages = 3;              // V runs one tile deeper than K: PV waits on it latest
+constexpr int kV = kK + 2 * kTileBytes;  // 2 K stages
+constexpr int kP = kV + kVStages * kTileBytes;
+constexpr int kBars = kP + kTileBytes;
+// barriers: q_full, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], s_empty[2], p_full, o_done
+constexpr int kNumBars = 1 + 2 + 2 + 3 + 3 + 2 + 2 + 1 + 1;
 constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 
@@ -71,11 +67,11 @@ struct Bars {
     __device__ uint64_t* k_full(int i) const { return base + 1 + i; }
     __device__ uint64_t* k_empty(int i) const { return base + 3 + i; }
     __device__ uint64_t* v_full(int i) const { return base + 5 + i; }
-    __device__ uint64_t* v_empty(int i) const { return base + 7 + i; }
-    __device__ uint64_t* s_full(int i) const { return base + 9 + i; }
-    __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
-    __device__ uint64_t* p_full() const { return base + 13; }
-    __device__ uint64_t* o_done() const { return base + 14; }
+    __device__ uint64_t* v_empty(int i) const { return base + 8 + i; }
+    __device__ uint64_t* s_full(int i) const { return base + 11 + i; }
+    __device__ uint64_t* s_empty(int i) const { return base + 13 + i; }
+    __device__ uint64_t* p_full() const { return base + 15; }
+    __device__ uint64_t* o_done() const { return base + 16; }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -113,7 +109,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Bars bars{reinterpret_cast<uint64_t*>(smem + kBars)};
-    VInfo* vinfo = reinterpret_cast<VInfo*>(smem + kInfo);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -122,10 +117,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.k_full(i), 1);
             mbar_init(bars.k_empty(i), 1);
-            mbar_init(bars.v_full(i), 1);
-            mbar_init(bars.v_empty(i), 1);
             mbar_init(bars.s_full(i), 1);
             mbar_init(bars.s_empty(i), 4);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(bars.v_full(i), 1);
+            mbar_init(bars.v_empty(i), 1);
         }
         mbar_init(bars.p_full(), 4);
         mbar_init(bars.o_done(), 1);
@@ -170,15 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            uint32_t vmask[4] = {0u, 0u, 0u, 0u};
             uint32_t bytes = 0;
             for (int b = 0; b < bpt; ++b) {
                 const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                if (b0 + b < nblk && pb >= 0) {
-                    bytes += 2u * B * 128u;
-                    for (int k = b * B; k < (b + 1) * B; ++k)
-                        if (j * kTileK + k < nkeys) vmask[k >> 5] |= 1u << (k & 31);
-                }
+                if (b0 + b < nblk && pb >= 0) bytes += 2u * B * 128u;
             }
             // K tile j
             if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
@@ -191,18 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < 2; ++h)
                     tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + lane * B * 128, &tmk, kvh * kD + h * 64,
                                 my_pb * B, bars.k_full(st));
-            // V tile j, with the validity of its keys
-            if (j >= 2 && !mbar_wait(bars.v_empty(st), ((j - 2) >> 1) & 1)) ok = false;
+            // V tile j
+            const int vs = j % kVStages;
+            if (j >= kVStages && !mbar_wait(bars.v_empty(vs), ((j / kVStages) - 1) & 1)) ok = false;
             if (!ok) break;
-            if (lane == 0) {
-                for (int w = 0; w < 4; ++w) vinfo[st].valid[w] = vmask[w];
-                mbar_arrive_expect_tx(bars.v_full(st), bytes);
-            }
+            if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
             __syncwarp();
             if (my_load)
                 for (int h = 0; h < 2; ++h)
-                    tma_load_2d(smem + kV + st * kTileBytes + h * kHalf + lane * B * 128, &tmv, kvh * kD + h * 64,
-                                my_pb * B, bars.v_full(st));
+                    tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + lane * B * 128, &tmv, kvh * kD + h * 64,
+                                my_pb * B, bars.v_full(vs));
             __syncwarp();
         }
         if (!ok && lane == 0) count_error(p.error_count);
@@ -232,11 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_commit(bars.k_empty(st));
                 }
                 if (j >= 1) {  // O += P_{j-1} V_{j-1}
-                    const int jj = j - 1, st = jj & 1;
+                    const int jj = j - 1, vs = jj % kVStages;
                     if (!mbar_wait(bars.p_full(), jj & 1)) { ok = false; break; }
-                    if (!mbar_wait(bars.v_full(st), (jj >> 1) & 1)) { ok = false; break; }
+                    if (!mbar_wait(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t vb = v_base + st * kTileBytes;
+                    const uint32_t vb = v_base + vs * kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
                         const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -244,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, jj > 0 || kk > 0);
                     }
                     umma_commit(bars.o_done());
-                    umma_commit(bars.v_empty(st));
+                    umma_commit(bars.v_empty(vs));
                 }
             }
             if (!ok) count_error(p.error_count);
@@ -259,12 +249,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = pos - i0 < nq;
         const int my_last = min(start + pos, last_key);  // last key this row may see
         const float sl2 = p.scale_log2;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        const int nblk = (nkeys + B - 1) / B;
+        const int bpt = kTileK / B;
         float m_run = -INFINITY, l_run = 0.f;
         uint8_t* p_tile = smem + kP;
         for (int j = 0; j < nt && ok; ++j) {
             const int st = j & 1;
+            // validity of the tile's 128 keys: inside the context and in a block with a valid table entry
+            uint32_t vm[4] = {0u, 0u, 0u, 0u};
+            for (int b = 0; b < bpt; ++b) {
+                const int lb = j * bpt + b;
+                if (lb >= nblk) break;
+                const int pb = table[lb];
+                if (pb < 0 || pb >= p.num_blocks) continue;
+                const int k0 = b * B, k1 = min((b + 1) * B, nkeys - j * kTileK);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
+                    if (lo < hi) vm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                }
+            }
             if (!mbar_wait(bars.s_full(st), (j >> 1) & 1)) { ok = false; break; }
-            if (!mbar_wait(bars.v_full(st), (j >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             float sv[kTileK];
 #pragma unroll
@@ -278,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.s_empty(st));
-            const uint32_t vm[4] = {vinfo[st].valid[0], vinfo[st].valid[1], vinfo[st].valid[2], vinfo[st].valid[3]};
             const int kbase = j * kTileK;
             float mt = -INFINITY;
 #pragma unroll
@@ -328,9 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(p_tile + (ch >> 3) * kHalf + swz(r, ch & 7)) = pk;
             }
             l_run += lsum;
-            // V row r carries no valid key for any row: zero it (stale or non-finite pool bytes)
+            // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
+            // bytes); only then does this tile need its V to have landed here
+            const bool need_zero = (vm[0] & vm[1] & vm[2] & vm[3]) != ~0u;
+            const int vs = j % kVStages;
+            if (need_zero && !mbar_wait(bars.v_full(vs), (j / kVStages) & 1)) { ok = false; break; }
             if (!((vm[r >> 5] >> (r & 31)) & 1u)) {
-                uint8_t* vrow = smem + kV + st * kTileBytes;
+                uint8_t* vrow = smem + kV + vs * kTileBytes;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
