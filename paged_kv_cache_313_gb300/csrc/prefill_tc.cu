@@ -13,16 +13,17 @@
 // Key tiles are 128 keys, gathered block by block from the pool by TMA
 // (one box per physical block and 64-column half, 128-byte swizzled).
 //
-// Warp roles (192 threads):
-//   warp 0    TMA producer: the Q tile once, then K tiles into a 2-deep and
-//             V tiles into a 3-deep ring; K and V are released separately (K
-//             after its QK^T MMA, V after its PV MMA) so loads run ahead.
+// Warp roles (320 threads):
+//   warp 0    TMA producer: the Q tile once, then K and V tiles into two
+//             2-deep rings; K and V are released separately (K after its
+//             QK^T MMA, V after its PV MMA) so loads run ahead.
 //   warp 1    TMEM owner and MMA issuer (one thread):
 //               S_j = Q K_j^T      M=128 N=128 K=128   -> TMEM S[j%2]
 //               O  += P_j V_j      M=128 N=128 K=128   -> TMEM O
 //             S is double-buffered, so QK^T of tile j+1 runs on the tensor
 //             cores while the softmax warps work on tile j.
-//   warps 2-5 softmax, one query row per thread (TMEM lane = row): read S,
+//   warps 2-9 softmax, two threads per query row (TMEM lane = row, 64
+//             columns each, maxima exchanged in shared memory): read S,
 //             mask (causal and context), online softmax in base-2 units with
 //             a lazy rescale (O in TMEM is rescaled only when the row max
 //             grows by more than 2^8), write P as bf16 into a swizzled shared
@@ -41,25 +42,29 @@ constexpr int kTileK = 128;      // keys per tile
 constexpr int kD = 128;          // head_dim handled by this kernel
 constexpr int kHalf = 128 * 128; // bytes of one 64-column half of a 128-row tile
 constexpr int kTileBytes = 2 * kHalf;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
 constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | unused
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kQ = 0;
 constexpr int kK = kQ + kTileBytes;      // 2 stages
-constexpr int kVStages = 3;              // V runs one tile deeper than K: PV waits on it latest
+constexpr int kVStages = 2;
 constexpr int kV = kK + 2 * kTileBytes;  // 2 K stages
 constexpr int kP = kV + kVStages * kTileBytes;
 constexpr int kBars = kP + kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], s_empty[2], p_full, o_done
-constexpr int kNumBars = 1 + 2 + 2 + 3 + 3 + 2 + 2 + 1 + 1;
-constexpr int kTmemSlot = kBars + kNumBars * 8;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, o_done
+constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr int kXchg = kBars + kNumBars * 8;        // float [2][2][128] maxima, [2][128] sums
+constexpr int kTmemSlot = kXchg + (2 * 2 + 2) * 128 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
+
+// the eight softmax warps (256 threads) only
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
 struct Bars {
     uint64_t* base;
@@ -67,11 +72,11 @@ struct Bars {
     __device__ uint64_t* k_full(int i) const { return base + 1 + i; }
     __device__ uint64_t* k_empty(int i) const { return base + 3 + i; }
     __device__ uint64_t* v_full(int i) const { return base + 5 + i; }
-    __device__ uint64_t* v_empty(int i) const { return base + 8 + i; }
-    __device__ uint64_t* s_full(int i) const { return base + 11 + i; }
-    __device__ uint64_t* s_empty(int i) const { return base + 13 + i; }
-    __device__ uint64_t* p_full() const { return base + 15; }
-    __device__ uint64_t* o_done() const { return base + 16; }
+    __device__ uint64_t* v_empty(int i) const { return base + 7 + i; }
+    __device__ uint64_t* s_full(int i) const { return base + 9 + i; }
+    __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
+    __device__ uint64_t* p_full() const { return base + 13; }
+    __device__ uint64_t* o_done() const { return base + 14; }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -118,13 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.k_full(i), 1);
             mbar_init(bars.k_empty(i), 1);
             mbar_init(bars.s_full(i), 1);
-            mbar_init(bars.s_empty(i), 4);
+            mbar_init(bars.s_empty(i), 8);
         }
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(bars.v_full(i), 1);
             mbar_init(bars.v_empty(i), 1);
         }
-        mbar_init(bars.p_full(), 4);
+        mbar_init(bars.p_full(), 8);
         mbar_init(bars.o_done(), 1);
         fence_mbar_init();
     }
@@ -242,9 +247,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ============================================================ softmax / epilogue
+        // Eight warps: warps 2-5 take columns 0-63 of every row, warps 6-9 columns
+        // 64-127.  The two threads of a row exchange their partial maxima (and, at
+        // the end, their partial sums) through shared memory.  Every thread runs
+        // every iteration and every named barrier, even after a wait timed out, so
+        // the barrier can never be left one-sided.
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
-        const int r = quarter * 32 + lane;  // the query row this thread owns
+        const int half = (warp - 2) >> 2;   // which 64 columns of the row
+        const int r = quarter * 32 + lane;  // the query row this thread works on
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int col0 = half * 64;
         const int pos = i0 + r / G;  // chunk-relative position
         const bool row_ok = pos - i0 < nq;
         const int my_last = min(start + pos, last_key);  // last key this row may see
@@ -252,9 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         const int nblk = (nkeys + B - 1) / B;
         const int bpt = kTileK / B;
+        float* xmax = reinterpret_cast<float*>(smem + kXchg);  // [tile parity][half][row]
+        float* xsum = xmax + 2 * 2 * kTileQ;                   // [half][row]
         float m_run = -INFINITY, l_run = 0.f;
         uint8_t* p_tile = smem + kP;
-        for (int j = 0; j < nt && ok; ++j) {
+        for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
             // validity of the tile's 128 keys: inside the context and in a block with a valid table entry
             uint32_t vm[4] = {0u, 0u, 0u, 0u};
@@ -270,30 +284,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lo < hi) vm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
                 }
             }
-            if (!mbar_wait(bars.s_full(st), (j >> 1) & 1)) { ok = false; break; }
+            if (ok && !mbar_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
             tc_fence_after();
-            float sv[kTileK];
+            float sv[64];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q2 = 0; q2 < 2; ++q2) {
                 float t[32];
-                tmem_ld32(tmem + lane_off + st * 128 + q4 * 32, t);
+                tmem_ld32(tmem + lane_off + st * 128 + col0 + q2 * 32, t);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sv[q4 * 32 + i] = t[i];
+                for (int i = 0; i < 32; ++i) sv[q2 * 32 + i] = t[i];
             }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.s_empty(st));
-            const int kbase = j * kTileK;
-            float mt = -INFINITY;
+            if (lane == 0 && ok) mbar_arrive(bars.s_empty(st));
+            const int kbase = j * kTileK + col0;
+            const uint32_t w0 = vm[half * 2], w1 = vm[half * 2 + 1];
+            // dense: every key of my 64 is valid and causally visible, and the scale is positive,
+            // so the max can be taken on raw scores and the scale folded into one FMA later
+            const bool dense = (w0 & w1) == ~0u && kbase + 63 <= my_last && sl2 > 0.f;
+            float mpart = -INFINITY;
+            if (dense) {
 #pragma unroll
-            for (int k = 0; k < kTileK; ++k) {
-                const bool valid = ((vm[k >> 5] >> (k & 31)) & 1u) && kbase + k <= my_last;
-                sv[k] = valid ? sv[k] * sl2 : -INFINITY;
-                mt = fmaxf(mt, sv[k]);
+                for (int k = 0; k < 64; ++k) mpart = fmaxf(mpart, sv[k]);
+                mpart *= sl2;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 64; ++k) {
+                    const bool valid = (((k < 32 ? w0 : w1) >> (k & 31)) & 1u) && kbase + k <= my_last;
+                    sv[k] = valid ? sv[k] * sl2 : -INFINITY;
+                    mpart = fmaxf(mpart, sv[k]);
+                }
             }
+            xmax[((j & 1) * 2 + half) * kTileQ + r] = mpart;
+            softmax_bar();
+            const float mt = fmaxf(mpart, xmax[((j & 1) * 2 + (half ^ 1)) * kTileQ + r]);
             // PV_{j-1} must be complete before O is rescaled or P overwritten
-            if (j > 0 && !mbar_wait(bars.o_done(), (j - 1) & 1)) { ok = false; break; }
+            if (j > 0 && ok && !mbar_wait(bars.o_done(), (j - 1) & 1)) ok = false;
             tc_fence_after();
             if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
                 if (m_run != -INFINITY) {
@@ -301,28 +328,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l_run *= alpha;
                     if (j > 0) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
+                        for (int q2 = 0; q2 < 2; ++q2) {
                             float t[32];
-                            tmem_ld32(tmem + lane_off + 256 + q4 * 32, t);
+                            tmem_ld32(tmem + lane_off + 256 + col0 + q2 * 32, t);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) t[i] *= alpha;
-                            tmem_st32(tmem + lane_off + 256 + q4 * 32, t);
+                            tmem_st32(tmem + lane_off + 256 + col0 + q2 * 32, t);
                         }
                         tmem_wait_st();
                     }
                 }
                 m_run = mt;
             }
-            // P = 2^(x - m) in bf16, written to the swizzled shared tile (row r)
+            // P = 2^(x - m) in bf16, my 64 columns of row r in the swizzled shared tile
             float lsum = 0.f;
+            const float neg_m = -m_run;
 #pragma unroll
-            for (int ch = 0; ch < kTileK / 8; ++ch) {
+            for (int cc = 0; cc < 8; ++cc) {
                 float e[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float x = sv[ch * 8 + i];
-                    e[i] = (x == -INFINITY) ? 0.f : fast_exp2(x - m_run);
+                    const float x = sv[cc * 8 + i];
+                    if (dense)
+                        e[i] = fast_exp2(fmaf(x, sl2, neg_m));
+                    else
+                        e[i] = (x == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x + neg_m);
                     lsum += e[i];
                 }
                 uint4 pk;
@@ -330,15 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk.y = pack_bf16x2(e[2], e[3]);
                 pk.z = pack_bf16x2(e[4], e[5]);
                 pk.w = pack_bf16x2(e[6], e[7]);
-                *reinterpret_cast<uint4*>(p_tile + (ch >> 3) * kHalf + swz(r, ch & 7)) = pk;
+                *reinterpret_cast<uint4*>(p_tile + half * kHalf + swz(r, cc)) = pk;
             }
             l_run += lsum;
             // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
             // bytes); only then does this tile need its V to have landed here
             const bool need_zero = (vm[0] & vm[1] & vm[2] & vm[3]) != ~0u;
             const int vs = j % kVStages;
-            if (need_zero && !mbar_wait(bars.v_full(vs), (j / kVStages) & 1)) { ok = false; break; }
-            if (!((vm[r >> 5] >> (r & 31)) & 1u)) {
+            if (need_zero && ok && !mbar_wait(bars.v_full(vs), (j / kVStages) & 1)) ok = false;
+            if (need_zero && ok && half == 0 && !((vm[r >> 5] >> (r & 31)) & 1u)) {
                 uint8_t* vrow = smem + kV + vs * kTileBytes;
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -349,20 +380,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full());
+            if (lane == 0 && ok) mbar_arrive(bars.p_full());
         }
-        // ---- epilogue: O / l -> out
+        // ---- epilogue: O / l -> out (each thread stores its 64 columns of the row)
         if (ok && nt > 0 && !mbar_wait(bars.o_done(), (nt - 1) & 1)) ok = false;
         tc_fence_after();
         if (!ok && lane == 0) count_error(p.error_count);
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        xsum[half * kTileQ + r] = l_run;
+        softmax_bar();
+        const float l_row = l_run + xsum[(half ^ 1) * kTileQ + r];
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                             ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD;
+                             ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD + col0;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
             float t[32];
             if (nt > 0) {
-                tmem_ld32(tmem + lane_off + 256 + q4 * 32, t);
+                tmem_ld32(tmem + lane_off + 256 + col0 + q2 * 32, t);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -376,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk.y = pack_bf16x2(t[i + 2] * inv, t[i + 3] * inv);
                     pk.z = pack_bf16x2(t[i + 4] * inv, t[i + 5] * inv);
                     pk.w = pack_bf16x2(t[i + 6] * inv, t[i + 7] * inv);
-                    *reinterpret_cast<uint4*>(out + q4 * 32 + i) = pk;
+                    *reinterpret_cast<uint4*>(out + q2 * 32 + i) = pk;
                 }
             }
         }
