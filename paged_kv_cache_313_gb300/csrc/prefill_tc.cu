@@ -344,16 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P = 2^(x - m) in bf16, my 64 columns of row r in the swizzled shared tile
             float lsum = 0.f;
             const float neg_m = -m_run;
+            if (dense) {
+#pragma unroll
+                for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
+            } else {
+#pragma unroll
+                for (int k = 0; k < 64; ++k)
+                    sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
+            }
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 float e[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float x = sv[cc * 8 + i];
-                    if (dense)
-                        e[i] = fast_exp2(fmaf(x, sl2, neg_m));
-                    else
-                        e[i] = (x == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(x + neg_m);
+                    e[i] = sv[cc * 8 + i];
                     lsum += e[i];
                 }
                 uint4 pk;
