@@ -23,11 +23,12 @@
 //             S is double-buffered, so QK^T of tile j+1 runs on the tensor
 //             cores while the softmax warps work on tile j.
 //   warps 2-9 softmax, two threads per query row (TMEM lane = row, 64
-//             columns each, maxima exchanged in shared memory): read S,
+//             columns each, maxima exchanged through spare TMEM columns): read S,
 //             mask (causal and context), online softmax in base-2 units with
 //             a lazy rescale (O in TMEM is rescaled only when the row max
-//             grows by more than 2^8), write P as bf16 into a swizzled shared
-//             tile for the PV MMA, zero V rows past the last valid key, and
+//             grows by more than 2^8), write P as bf16 into one of two swizzled
+//             shared tiles for the PV MMA (so tile j+1 needs PV_j only when O
+//             must be rescaled), zero V rows past the last valid key, and
 //             finally normalise O and store the output rows.
 // All waits are bounded (an error is counted and the kernel still finishes);
 // TMEM is always freed.
@@ -43,7 +44,8 @@ constexpr int kD = 128;          // head_dim handled by this kernel
 constexpr int kHalf = 128 * 128; // bytes of one 64-column half of a 128-row tile
 constexpr int kTileBytes = 2 * kHalf;
 constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
-constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | unused
+constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | row exchange (6 columns) | unused
+constexpr uint32_t kTmemXchg = 384;        // [tile parity][half] partial maxima, then [half] partial sums
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
 // shared memory layout (offsets from a 1024-aligned base)
@@ -51,12 +53,11 @@ constexpr int kQ = 0;
 constexpr int kK = kQ + kTileBytes;      // 2 stages
 constexpr int kVStages = 2;
 constexpr int kV = kK + 2 * kTileBytes;  // 2 K stages
-constexpr int kP = kV + kVStages * kTileBytes;
-constexpr int kBars = kP + kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, o_done
-constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
-constexpr int kXchg = kBars + kNumBars * 8;        // float [2][2][128] maxima, [2][128] sums
-constexpr int kTmemSlot = kXchg + (2 * 2 + 2) * 128 * 4;
+constexpr int kP = kV + kVStages * kTileBytes;  // 2 P buffers
+constexpr int kBars = kP + 2 * kTileBytes;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], o_done[2]
+constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
+constexpr int kTmemSlot = kBars + kNumBars * 8;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -75,8 +76,8 @@ struct Bars {
     __device__ uint64_t* v_empty(int i) const { return base + 7 + i; }
     __device__ uint64_t* s_full(int i) const { return base + 9 + i; }
     __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
-    __device__ uint64_t* p_full() const { return base + 13; }
-    __device__ uint64_t* o_done() const { return base + 14; }
+    __device__ uint64_t* p_full(int i) const { return base + 13 + i; }  // P buffer i written
+    __device__ uint64_t* o_done(int i) const { return base + 15 + i; }  // the PV that read P buffer i is done
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,8 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.v_full(i), 1);
             mbar_init(bars.v_empty(i), 1);
         }
-        mbar_init(bars.p_full(), 8);
-        mbar_init(bars.o_done(), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.p_full(i), 8);
+            mbar_init(bars.o_done(i), 1);
+        }
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -209,6 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
             const uint32_t v_base = smem_u32(smem + kV), p_base = smem_u32(smem + kP);
             const uint32_t t_o = tmem + 256;
+            // descriptors of k-step 0; a k-step adds its byte offset >> 4 to the start-address field
+            const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
+            const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
+            const uint64_t dp0 = umma_desc_sw128(p_base, 16, 1024);
+            const uint64_t dv0 = umma_desc_sw128(v_base, kHalf, 1024);
             if (nt > 0 && !mbar_wait(bars.q_full(), 0)) ok = false;
             for (int j = 0; j <= nt && ok; ++j) {
                 if (j < nt) {  // S_j = Q K_j^T into S[j%2]
@@ -216,29 +224,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(bars.k_full(st), (j >> 1) & 1)) { ok = false; break; }
                     if (j >= 2 && !mbar_wait(bars.s_empty(st), ((j - 2) >> 1) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t kb = k_base + st * kTileBytes;
+                    const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma_bf16(tmem + st * 128, umma_desc_sw128(q_base + off, 16, 1024),
-                                  umma_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+                        const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                        umma_bf16(tmem + st * 128, dq0 + off, dk + off, idesc_s, kk > 0);
                     }
                     umma_commit(bars.s_full(st));
                     umma_commit(bars.k_empty(st));
                 }
                 if (j >= 1) {  // O += P_{j-1} V_{j-1}
-                    const int jj = j - 1, vs = jj % kVStages;
-                    if (!mbar_wait(bars.p_full(), jj & 1)) { ok = false; break; }
+                    const int jj = j - 1, vs = jj % kVStages, pb = jj & 1;
+                    if (!mbar_wait(bars.p_full(pb), (jj >> 1) & 1)) { ok = false; break; }
                     if (!mbar_wait(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t vb = v_base + vs * kTileBytes;
+                    const uint64_t dp = dp0 + (uint64_t)((pb * kTileBytes) >> 4);
+                    const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma_bf16(t_o, umma_desc_sw128(p_base + poff, 16, 1024),
-                                  umma_desc_sw128(vb + kk * 2048, kHalf, 1024), idesc_o, jj > 0 || kk > 0);
+                        const uint64_t poff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                        umma_bf16(t_o, dp + poff, dv + (uint64_t)((kk * 2048) >> 4), idesc_o, jj > 0 || kk > 0);
                     }
-                    umma_commit(bars.o_done());
+                    umma_commit(bars.o_done(pb));
                     umma_commit(bars.v_empty(vs));
                 }
             }
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================ softmax / epilogue
         // Eight warps: warps 2-5 take columns 0-63 of every row, warps 6-9 columns
         // 64-127.  The two threads of a row exchange their partial maxima (and, at
-        // the end, their partial sums) through shared memory.  Every thread runs
+        // the end, their partial sums) through spare TMEM columns.  Every thread runs
         // every iteration and every named barrier, even after a wait timed out, so
         // the barrier can never be left one-sided.
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
@@ -264,8 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         const int nblk = (nkeys + B - 1) / B;
         const int bpt = kTileK / B;
-        float* xmax = reinterpret_cast<float*>(smem + kXchg);  // [tile parity][half][row]
-        float* xsum = xmax + 2 * 2 * kTileQ;                   // [half][row]
         float m_run = -INFINITY, l_run = 0.f;
         uint8_t* p_tile = smem + kP;
         for (int j = 0; j < nt; ++j) {
@@ -316,17 +321,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mpart = fmaxf(mpart, sv[k]);
                 }
             }
-            xmax[((j & 1) * 2 + half) * kTileQ + r] = mpart;
+            // the row's two halves exchange partial maxima through a spare TMEM column pair
+            tmem_st1(tmem + lane_off + kTmemXchg + (j & 1) * 2 + half, mpart);
+            tmem_wait_st();
+            tc_fence_before();
             softmax_bar();
-            const float mt = fmaxf(mpart, xmax[((j & 1) * 2 + (half ^ 1)) * kTileQ + r]);
-            // PV_{j-1} must be complete before O is rescaled or P overwritten
-            if (j > 0 && ok && !mbar_wait(bars.o_done(), (j - 1) & 1)) ok = false;
             tc_fence_after();
+            const float mt = fmaxf(mpart, tmem_ld1(tmem + lane_off + kTmemXchg + (j & 1) * 2 + (half ^ 1)));
+            tmem_wait_ld();
             if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
                 if (m_run != -INFINITY) {
                     const float alpha = fast_exp2(m_run - mt);
                     l_run *= alpha;
                     if (j > 0) {
+                        // every PV issued so far (the last is PV_{j-1}) must be done before O changes
+                        if (ok && !mbar_wait(bars.o_done((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
+                        tc_fence_after();
 #pragma unroll
                         for (int q2 = 0; q2 < 2; ++q2) {
                             float t[32];
@@ -341,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_run = mt;
             }
-            // P = 2^(x - m) in bf16, my 64 columns of row r in the swizzled shared tile
+            // P = 2^(x - m) in bf16, my 64 columns of row r in P buffer j%2, which PV_{j-2} read
+            if (j >= 2 && ok && !mbar_wait(bars.o_done(j & 1), ((j - 2) >> 1) & 1)) ok = false;
+            tc_fence_after();
+            uint8_t* p_buf = p_tile + (j & 1) * kTileBytes;
             float lsum = 0.f;
             const float neg_m = -m_run;
             if (dense) {
@@ -365,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk.y = pack_bf16x2(e[2], e[3]);
                 pk.z = pack_bf16x2(e[4], e[5]);
                 pk.w = pack_bf16x2(e[6], e[7]);
-                *reinterpret_cast<uint4*>(p_tile + half * kHalf + swz(r, cc)) = pk;
+                *reinterpret_cast<uint4*>(p_buf + half * kHalf + swz(r, cc)) = pk;
             }
             l_run += lsum;
             // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
@@ -384,15 +397,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(bars.p_full());
+            if (lane == 0 && ok) mbar_arrive(bars.p_full(j & 1));
         }
         // ---- epilogue: O / l -> out (each thread stores its 64 columns of the row)
-        if (ok && nt > 0 && !mbar_wait(bars.o_done(), (nt - 1) & 1)) ok = false;
+        if (ok && nt > 0 && !mbar_wait(bars.o_done((nt - 1) & 1), ((nt - 1) >> 1) & 1)) ok = false;
         tc_fence_after();
         if (!ok && lane == 0) count_error(p.error_count);
-        xsum[half * kTileQ + r] = l_run;
+        tmem_st1(tmem + lane_off + kTmemXchg + 4 + half, l_run);
+        tmem_wait_st();
+        tc_fence_before();
         softmax_bar();
-        const float l_row = l_run + xsum[(half ^ 1) * kTileQ + r];
+        tc_fence_after();
+        const float l_row = l_run + tmem_ld1(tmem + lane_off + kTmemXchg + 4 + (half ^ 1));
+        tmem_wait_ld();
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
                              ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD + col0;
