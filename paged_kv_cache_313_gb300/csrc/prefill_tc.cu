@@ -55,9 +55,11 @@ constexpr int kVStages = 2;
 constexpr int kV = kK + 2 * kTileBytes;  // 2 K stages
 constexpr int kP = kV + kVStages * kTileBytes;  // 2 P buffers
 constexpr int kBars = kP + 2 * kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], o_done[2]
-constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
-constexpr int kTmemSlot = kBars + kNumBars * 8;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], o_done[2],
+// m_full[4]
+constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 4;
+constexpr int kMask = kBars + kNumBars * 8;  // uint32 [4][4]: key-validity mask of tile j in slot j%4
+constexpr int kTmemSlot = kMask + 4 * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -78,6 +80,7 @@ struct Bars {
     __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
     __device__ uint64_t* p_full(int i) const { return base + 13 + i; }  // P buffer i written
     __device__ uint64_t* o_done(int i) const { return base + 15 + i; }  // the PV that read P buffer i is done
+    __device__ uint64_t* m_full(int i) const { return base + 17 + i; }  // mask slot i published
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Bars bars{reinterpret_cast<uint64_t*>(smem + kBars)};
+    uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + kMask);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTmemSlot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -134,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.p_full(i), 8);
             mbar_init(bars.o_done(i), 1);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(bars.m_full(i), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -175,14 +180,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            uint32_t bytes = 0;
+            uint32_t bytes = 0, vm[4] = {0u, 0u, 0u, 0u};
             for (int b = 0; b < bpt; ++b) {
                 const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                if (b0 + b < nblk && pb >= 0) bytes += 2u * B * 128u;
+                if (b0 + b < nblk && pb >= 0) {
+                    bytes += 2u * B * 128u;
+                    const int k0 = b * B, k1 = min((b + 1) * B, nkeys - j * kTileK);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
+                        if (lo < hi) vm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                    }
+                }
             }
-            // K tile j
+            // K tile j (its slot is free once S_{j-2} completed, which also means the softmax warps
+            // have read mask j-4: they read a mask before releasing that tile's S)
             if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
             if (!ok) break;
+            if (lane == 0) {
+                for (int w = 0; w < 4; ++w) vmask[(j & 3) * 4 + w] = vm[w];
+                mbar_arrive(bars.m_full(j & 3));
+            }
             if (lane == 0) mbar_arrive_expect_tx(bars.k_full(st), bytes);
             __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
             const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
@@ -268,27 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = pos - i0 < nq;
         const int my_last = min(start + pos, last_key);  // last key this row may see
         const float sl2 = p.scale_log2;
-        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-        const int nblk = (nkeys + B - 1) / B;
-        const int bpt = kTileK / B;
         float m_run = -INFINITY, l_run = 0.f;
         uint8_t* p_tile = smem + kP;
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
-            // validity of the tile's 128 keys: inside the context and in a block with a valid table entry
-            uint32_t vm[4] = {0u, 0u, 0u, 0u};
-            for (int b = 0; b < bpt; ++b) {
-                const int lb = j * bpt + b;
-                if (lb >= nblk) break;
-                const int pb = table[lb];
-                if (pb < 0 || pb >= p.num_blocks) continue;
-                const int k0 = b * B, k1 = min((b + 1) * B, nkeys - j * kTileK);
+            // validity of the tile's 128 keys (inside the context, in a block with a valid table
+            // entry), published by the producer
+            if (ok && !mbar_wait(bars.m_full(j & 3), (j >> 2) & 1)) ok = false;
+            uint32_t vm[4];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
-                    if (lo < hi) vm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
-                }
-            }
+            for (int w = 0; w < 4; ++w) vm[w] = vmask[(j & 3) * 4 + w];
             if (ok && !mbar_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
             tc_fence_after();
             float sv[64];
