@@ -13,10 +13,12 @@
 // Key tiles are 128 keys, gathered block by block from the pool by TMA
 // (one box per physical block and 64-column half, 128-byte swizzled).
 //
-// Warp roles (320 threads):
-//   warp 0    TMA producer: the Q tile once, then K and V tiles into two
-//             2-deep rings; K and V are released separately (K after its
-//             QK^T MMA, V after its PV MMA) so loads run ahead.
+// Warp roles (352 threads):
+//   warp 0    TMA producer of the Q tile (once) and of K tiles into a 2-deep
+//             ring (released after their QK^T MMA); it also publishes each
+//             key tile's validity mask to the softmax warps.
+//   warp 10   TMA producer of V tiles into a 2-deep ring (released after their
+//             PV MMA); separate from warp 0 so K never queues behind V.
 //   warp 1    TMEM owner and MMA issuer (one thread):
 //               S_j = Q K_j^T      M=128 N=128 K=128   -> TMEM S[j%2]
 //               O  += P_j V_j      M=128 N=128 K=128   -> TMEM O
@@ -43,7 +45,8 @@ constexpr int kTileK = 128;      // keys per tile
 constexpr int kD = 128;          // head_dim handled by this kernel
 constexpr int kHalf = 128 * 128; // bytes of one 64-column half of a 128-row tile
 constexpr int kTileBytes = 2 * kHalf;
-constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
+constexpr int kThreads = 352;  // K producer, MMA issuer, 8 softmax warps, V producer
+constexpr int kVWarp = 10;
 constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | row exchange (6 columns) | unused
 constexpr uint32_t kTmemXchg = 384;        // [tile parity][half] partial maxima, then [half] partial sums
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
@@ -151,22 +154,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp == 0) {
-        // ============================================================ producer
+    if (warp == 0 || warp == kVWarp) {
+        // ============================================================ producers
+        // warp 0 loads Q, the K tiles and publishes each tile's key mask; warp kVWarp loads the V
+        // tiles.  Each waits only on its own ring, so K streams ahead of V.
+        const bool v_side = warp == kVWarp;
         const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         const int nblk = (nkeys + B - 1) / B;
         const int bpt = kTileK / B;  // blocks per key tile
-        if (lane == 0 && nt > 0) {  // with no keys nothing is loaded (and nothing may be left in flight)
+        if (!v_side && lane == 0 && nt > 0) {  // with no keys nothing is loaded (nor left in flight)
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
             mbar_arrive_expect_tx(bars.q_full(), 2 * kHalf);
             for (int h = 0; h < 2; ++h)
                 tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, r0 + i0, bars.q_full());
         }
+        if (v_side && lane == 0 && nt > 0) tma_prefetch_desc(&tmv);
         int chunk = -1, pb_lane = -1;
         for (int j = 0; j < nt; ++j) {
-            const int st = j & 1;
             const int b0 = j * bpt;
             if ((b0 >> 5) != chunk) {  // a tile's blocks never straddle a 32-entry chunk
                 chunk = b0 >> 5;
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (idx < nblk) {
                     pb_lane = table[idx];
                     if (pb_lane < 0 || pb_lane >= p.num_blocks) {
-                        count_error(p.error_count);
+                        if (!v_side) count_error(p.error_count);
                         pb_lane = -1;
                     }
                 }
@@ -193,32 +198,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // K tile j (its slot is free once S_{j-2} completed, which also means the softmax warps
-            // have read mask j-4: they read a mask before releasing that tile's S)
-            if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
-            if (!ok) break;
-            if (lane == 0) {
-                for (int w = 0; w < 4; ++w) vmask[(j & 3) * 4 + w] = vm[w];
-                mbar_arrive(bars.m_full(j & 3));
-            }
-            if (lane == 0) mbar_arrive_expect_tx(bars.k_full(st), bytes);
-            __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
             const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
             const bool my_load = lane < bpt && b0 + lane < nblk && my_pb >= 0;
-            if (my_load)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + lane * B * 128, &tmk, kvh * kD + h * 64,
-                                my_pb * B, bars.k_full(st));
-            // V tile j
-            const int vs = j % kVStages;
-            if (j >= kVStages && !mbar_wait(bars.v_empty(vs), ((j / kVStages) - 1) & 1)) ok = false;
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
-            __syncwarp();
-            if (my_load)
-                for (int h = 0; h < 2; ++h)
-                    tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + lane * B * 128, &tmv, kvh * kD + h * 64,
-                                my_pb * B, bars.v_full(vs));
+            if (!v_side) {
+                // K tile j (its slot is free once S_{j-2} completed, which also means the softmax
+                // warps have read mask j-4: they read a mask before releasing that tile's S)
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
+                if (!ok) break;
+                if (lane == 0) {
+                    for (int w = 0; w < 4; ++w) vmask[(j & 3) * 4 + w] = vm[w];
+                    mbar_arrive(bars.m_full(j & 3));
+                    mbar_arrive_expect_tx(bars.k_full(st), bytes);
+                }
+                __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
+                if (my_load)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + lane * B * 128, &tmk,
+                                    kvh * kD + h * 64, my_pb * B, bars.k_full(st));
+            } else {
+                // V tile j (its slot is free once PV_{j-kVStages} completed)
+                const int vs = j % kVStages;
+                if (j >= kVStages && !mbar_wait(bars.v_empty(vs), ((j / kVStages) - 1) & 1)) ok = false;
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
+                __syncwarp();
+                if (my_load)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + lane * B * 128, &tmv,
+                                    kvh * kD + h * 64, my_pb * B, bars.v_full(vs));
+            }
             __syncwarp();
         }
         if (!ok && lane == 0) count_error(p.error_count);
