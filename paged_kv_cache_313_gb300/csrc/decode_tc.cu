@@ -48,7 +48,7 @@ namespace {
 
 // Ring depth and CTAs per SM (build-time knobs; the defaults are the measured best).
 #ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 2
+#define PA_DECODE_STAGES 3
 #endif
 #ifndef PA_DECODE_CTAS_PER_SM
 #define PA_DECODE_CTAS_PER_SM 2
@@ -76,14 +76,18 @@ struct TcCfg {
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kRing = 0;
     static constexpr int kQ = kRing + kStages * kStageBytes;
-    static constexpr int kOred = kQ + kStages * kQBytes;                // [warp][head][D] float
-    static constexpr int kWmerge = kOred + kConsumerWarps * 8 * D * 4;  // [head][128] float
-    static constexpr int kCum = kWmerge + 8 * 128 * 4;                  // int [kMaxSeqs + 1]
+    // [head][D] float: the consumer warps' outputs are summed into it one warp at a time; the
+    // merge weights [head][max_splits <= 128] reuse it afterwards
+    static constexpr int kOred = kQ + kStages * kQBytes;
+    static constexpr int kWmerge = kOred;
+    static constexpr int kOredBytes = (8 * D > 8 * 128 ? 8 * D : 8 * 128) * 4;
+    static constexpr int kCum = kOred + kOredBytes;                     // int [kMaxSeqs + 1]
     static constexpr int kInfo = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
     static constexpr int kEnd = kBars + 2 * kStages * 8;
     static constexpr size_t kSmemBytes = 1024 + kEnd;
-    static_assert(kSmemBytes * PA_DECODE_CTAS_PER_SM <= 227 * 1024, "shared memory budget");
+    // an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA
+    static_assert((kSmemBytes + 1024) * PA_DECODE_CTAS_PER_SM <= 228 * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -414,16 +418,40 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             }
             const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
             const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
-            float* ored = reinterpret_cast<float*>(smem + C::kOred);
 #pragma unroll
             for (int mt = 0; mt < KT; ++mt) {
-                const int d = mt * 16 + g4;
-                ored[(warp * 8 + 2 * c4) * D + d] = o[mt][0] * f0;
-                ored[(warp * 8 + 2 * c4 + 1) * D + d] = o[mt][1] * f1;
-                ored[(warp * 8 + 2 * c4) * D + d + 8] = o[mt][2] * f0;
-                ored[(warp * 8 + 2 * c4 + 1) * D + d + 8] = o[mt][3] * f1;
+                o[mt][0] *= f0;
+                o[mt][1] *= f1;
+                o[mt][2] *= f0;
+                o[mt][3] *= f1;
             }
-            bar();
+            // sum the four warps' O^T through one [head][D] slab: warp 3 -> 2 -> 1 -> 0 -> slab
+            float* ored = reinterpret_cast<float*>(smem + C::kOred);
+            for (int w = C::kConsumerWarps - 1; w >= 0; --w) {
+                if (warp == w) {
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt) {
+                        const int d = mt * 16 + g4;
+                        ored[(2 * c4) * D + d] = o[mt][0];
+                        ored[(2 * c4 + 1) * D + d] = o[mt][1];
+                        ored[(2 * c4) * D + d + 8] = o[mt][2];
+                        ored[(2 * c4 + 1) * D + d + 8] = o[mt][3];
+                    }
+                }
+                bar();
+                if (w == 0) break;
+                if (warp == w - 1) {
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt) {
+                        const int d = mt * 16 + g4;
+                        o[mt][0] += ored[(2 * c4) * D + d];
+                        o[mt][1] += ored[(2 * c4 + 1) * D + d];
+                        o[mt][2] += ored[(2 * c4) * D + d + 8];
+                        o[mt][3] += ored[(2 * c4 + 1) * D + d + 8];
+                    }
+                }
+                bar();
+            }
             const size_t unit = decode_unit(p, inf.s, inf.kvh);
             __nv_bfloat16* out =
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;
@@ -433,13 +461,13 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[w][h]);
-                float Ls = 0.f, acc = 0.f;
+                float Ls = 0.f;
 #pragma unroll
                 for (int w = 0; w < C::kConsumerWarps; ++w) {
                     const float mw = red_m[w][h];
                     if (mw != -INFINITY) Ls += red_l[w][h] * fast_exp2(mw - M);
-                    acc += ored[(w * 8 + h) * D + d];
                 }
+                const float acc = ored[h * D + d];
                 const float val = Ls > 0.f ? acc / Ls : 0.f;
                 if (inf.nsplit == 1) {
                     out[idx] = __float2bfloat16_rn(val);

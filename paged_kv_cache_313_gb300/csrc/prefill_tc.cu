@@ -373,9 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* p_buf = p_tile + (j & 1) * kTileBytes;
             float lsum = 0.f;
             const float neg_m = -m_run;
-            if (dense) {
+            if (dense) {  // half the exponentials on the MUFU unit, half on the FMA pipe
 #pragma unroll
-                for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
+                for (int k = 0; k < 64; k += 2) {
+                    sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
+                    sv[k + 1] = poly_exp2(fmaf(sv[k + 1], sl2, neg_m));
+                }
             } else {
 #pragma unroll
                 for (int k = 0; k < 64; ++k)
