@@ -13,8 +13,10 @@ sequence per step) over all ranks, timed over exactly K steps, each a replay
 of the step captured as a CUDA graph (``--no-graph``: eager launches).  The
 roofline object describes the decode kernel (algorithmic K/V bytes per launch
 / its CUDA-event time over eager launches, against the measured HBM copy
-bandwidth).  ``e2e`` re-times the step eagerly through the public API with
-pinned-host inputs copied in and the outputs copied out inside the events.
+bandwidth).  ``e2e`` re-times the step through the public API from host
+memory: the step's packed inputs copied in from pinned memory (one copy), the
+step (graph replay unless ``--no-graph``), the packed outputs copied back (one
+copy), all inside the events.
 L2 is flushed (a 512 MiB write) before every timed step.  Under torchrun each
 rank runs an independent shard with its own seed (weak scaling, no collective
 on the data path).
@@ -187,12 +189,6 @@ def kv_memory(w):
     return {k: u[k] for k in keep}
 
 
-def step_input_tensors(step):
-    """The per-step inputs a serving loop hands to the path (the pools are resident state)."""
-    return [step.q_decode, step.k_new, step.v_new, step.block_tables, step.context_lens, step.seq_idx, step.pos,
-            step.q_prefill, step.cu_q_lens, step.q_start_pos, step.seq_of_chunk]
-
-
 # ---------------------------------------------------------- CPU oracle arm
 def oracle_step_time(w, target_seconds: float):
     """Time the oracle's full step (slot mapping, KV write, decode, prefill) on
@@ -343,23 +339,19 @@ def run_native(args):
     decode_ms = [e[1].elapsed_time(e[2]) for e in kev]
     prefill_ms = [e[2].elapsed_time(e[3]) for e in kev]
 
-    # ---- end to end through the public API: pinned host inputs -> device, step, output -> host
-    host_in = [t.detach().cpu().pin_memory() for t in step_input_tensors(step)]
-    host_out_d = torch.empty(step.out_decode.shape, dtype=step.out_decode.dtype).pin_memory()
-    host_out_p = torch.empty(step.out_prefill.shape, dtype=step.out_prefill.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out_d.numel() * host_out_d.element_size() + host_out_p.numel() * host_out_p.element_size()
+    # ---- end to end through the public API: the packed inputs copied in from
+    # pinned host memory (one copy), the step, the packed outputs copied back
+    host_in = step.pinned_inputs()
+    host_out = step.pinned_outputs()
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
     K2 = max(1, min(K, 50))
     for i in range(K2):
         flush.fill_(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for dst, src in zip(step_input_tensors(step), host_in):
-            dst.copy_(src, non_blocking=True)
-        step.run()
-        host_out_d.copy_(step.out_decode, non_blocking=True)
-        host_out_p.copy_(step.out_prefill, non_blocking=True)
+        step.run_from_host(host_in, host_out, graph=args.graph)
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
@@ -388,7 +380,8 @@ def run_native(args):
         "stage_ms": {"slot_mapping+write_kv": statistics.mean(write_ms), "decode": mean_dec,
                      "prefill": statistics.mean(prefill_ms)},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2, "launch": "eager"},
+                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2,
+                "launch": "cuda_graph" if args.graph else "eager"},
         "step_launch": "cuda_graph" if args.graph else "eager",
         "gpu_launches": K * launches_per_step,
         "kv_memory": kv_memory(w),

@@ -65,7 +65,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     int num_sms = 0;
     int rc = check_device(&num_sms);
     if (rc != PA_OK) return rc;
-    DecodePlan plan = plan_decode(num_seqs, num_kv_heads, max_context_len, num_sms);
+    DecodePlan plan =
+        plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, kNoAllocScratchBytes);
     DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
     if (lay.total > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;  // beyond the built-in 16 MiB
     void* scratch = nullptr;

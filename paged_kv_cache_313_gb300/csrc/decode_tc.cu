@@ -17,13 +17,13 @@
 // Inside a CTA:
 //  * Warp 4 is the producer.  It walks its items and, for each 64-token
 //    stage, resolves the stage's block-table entries (one coalesced warp load
-//    per 32 blocks) and issues one 2-D TMA copy per (block, 64-column half)
-//    of K and of V — a physical block of one kv head is B rows of head_dim
-//    contiguous bf16 at a row stride of Hkv*head_dim, a box of the pool
-//    viewed as a [P*B, Hkv*D] matrix — plus, on an item's first stage, a 1-D
-//    bulk copy of the item's G query rows.  Boxes land 128-byte swizzled
-//    (ldmatrix reads are bank-conflict free) in a ring of kStages stages,
-//    completion counted on mbarriers.  The producer streams straight across
+//    per 32 blocks) and issues one 3-D TMA copy per block of K and of V — a
+//    physical block of one kv head is B rows of head_dim contiguous bf16 at a
+//    row stride of Hkv*head_dim, one box {64 columns, B rows, D/64 halves}
+//    of the pool viewed as [128-byte segment][row][64] — plus, on an item's
+//    first stage, a 1-D bulk copy of the item's G query rows.  Boxes land
+//    128-byte swizzled (ldmatrix reads are bank-conflict free) in a ring of
+//    kStages stages, completion counted on mbarriers.  The producer streams straight across
 //    item boundaries, so there is no per-item start-up gap.
 //  * Warps 0-3 consume 16 tokens of each stage apiece.  The G <= 8 query
 //    heads form the N=8 side of m16n8k16 bf16 MMAs:
@@ -90,10 +90,19 @@ struct TcCfg {
     static_assert((kSmemBytes + 1024) * PA_DECODE_CTAS_PER_SM <= 228 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
-    // 128-byte swizzle: 16-byte chunk c of 128-byte row r sits at chunk c ^ (r & 7)
-    return row * 128u + ((chunk ^ (row & 7u)) << 4);
-}
+// Byte offset, within a stage's K (or V) tile, of 128-byte row r of half 0,
+// and the distance between the halves of a row.  The 128-byte swizzle of a
+// row depends on r & 7 either way: boxes start 1 KiB aligned and B >= 8.
+struct TileRows {
+    uint32_t half_stride, block_stride;
+    int log2b;
+    __device__ __forceinline__ uint32_t row(uint32_t r) const {
+        return (r >> log2b) * block_stride + (r & ((1u << log2b) - 1u)) * 128u;
+    }
+    __device__ __forceinline__ uint32_t at(uint32_t r, uint32_t half, uint32_t chunk) const {
+        return row(r) + half * half_stride + ((chunk ^ (r & 7u)) << 4);
+    }
+};
 
 struct ConsumerBarrier {
     __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -254,12 +263,9 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 uint8_t* vdst = kdst + C::kTileBytes;
                 const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
                 if (lane < nb && my_pb >= 0) {
-#pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h) {
-                        const int x = kvh * D + h * 64;
-                        tma_load_2d(kdst + h * C::kHalfBytes + lane * B * 128, &tmk, x, my_pb * B, &full[slot]);
-                        tma_load_2d(vdst + h * C::kHalfBytes + lane * B * 128, &tmv, x, my_pb * B, &full[slot]);
-                    }
+                    const int boff = lane * C::kHalves * B * 128;
+                    tma_load_3d(kdst + boff, &tmk, 0, my_pb * B, kvh * C::kHalves, &full[slot]);
+                    tma_load_3d(vdst + boff, &tmv, 0, my_pb * B, kvh * C::kHalves, &full[slot]);
                 }
                 __syncwarp();
                 ++stage_no;
@@ -292,6 +298,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         }
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*c4 and 2*c4+1
         const float sl2 = p.scale_log2;
+        const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kHalves * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
             const int slot = stage_no % C::kStages;
             if (!mbar_wait(&full[slot], (stage_no / C::kStages) & 1)) {
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<int4*>(vt + h * C::kHalfBytes + (row0 + r) * 128 +
+                                *reinterpret_cast<int4*>(vt + tr.row(row0 + r) + h * tr.half_stride +
                                                          ((lane & 1) * 4 + c) * 16) = z;
                     }
                     __syncwarp();
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     for (int kk = 0; kk < KT; ++kk) {
                         const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
                         uint32_t a[4];
-                        ldmatrix_x4(a, kbase + half * C::kHalfBytes + swz(r, ch));
+                        ldmatrix_x4(a, kbase + tr.at(r, half, ch));
                         if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
                         else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
                     }
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     for (int mt = 0; mt < KT; ++mt) {
                         const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
                         uint32_t a[4];
-                        ldmatrix_x4_trans(a, vbase + half * C::kHalfBytes + swz(r, ch));
+                        ldmatrix_x4_trans(a, vbase + tr.at(r, half, ch));
                         mma_bf16_16816(o[mt], a, b0, b1);
                     }
                 }
@@ -500,9 +507,9 @@ template <int D>
 int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     using C = TcCfg<D>;
     CUtensorMap tmk, tmv;
-    int rc = pool_tensor_map(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D);
+    int rc = pool_tensor_map_rows(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D);
     if (rc != PA_OK) return rc;
-    if ((rc = pool_tensor_map(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D)) != PA_OK) return rc;
+    if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D)) != PA_OK) return rc;
     if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D>), C::kSmemBytes)) != PA_OK)
         return rc;
     // PA_DECODE_CTAS_PER_SM CTAs per SM, never more CTAs than the largest possible item count
@@ -537,6 +544,25 @@ int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int bloc
     cuuint32_t box[2] = {64, (cuuint32_t)block_size};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
+// The pool as a 3-D map for one-box-per-block loads: x = column within a
+// 128-byte segment (64), y = pool row (P*B, stride Hkv*D*2 bytes), z = 128-byte
+// segment of the row (Hkv*D/64, stride 128 bytes).  A box {64, B, D/64} at
+// (0, pb*B, kvh*D/64) is block pb's B rows of kv head kvh, stored
+// [segment][row][64] and 128-byte swizzled.
+int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
+                         int head_dim) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return PA_ERR_CUDA;
+    cuuint64_t dims[3] = {64, (cuuint64_t)num_blocks * block_size, (cuuint64_t)num_kv_heads * head_dim / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)num_kv_heads * head_dim * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)block_size, (cuuint32_t)(head_dim / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;

@@ -1,6 +1,7 @@
 // pa_api.cu — the C ABI of libpa.so: argument checks, device checks and
 // dispatch to the kernels.  Every entry point validates on the host and
 // launches nothing when a check fails.
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 #include <set>
@@ -66,22 +67,6 @@ int ensure_dynamic_smem(const void* kernel, size_t bytes) {
     return PA_OK;
 }
 
-DecodePlan plan_decode(int num_seqs, int num_kv_heads, int max_context_len, int num_sms) {
-    // 512-token partitions keep each CTA's stream of K/V long enough to hide
-    // the pipeline fill; shrink them while the grid would not cover two waves
-    // of the GPU; grow them so that no (sequence, head) has more than 128
-    // partials to merge.
-    int partition = 512;
-    auto ctas = [&](int part) {
-        long long splits = (max_context_len + part - 1) / part;
-        return (long long)num_seqs * num_kv_heads * (splits < 1 ? 1 : splits);
-    };
-    while (partition > 64 && ctas(partition) < 2LL * num_sms) partition >>= 1;
-    while ((max_context_len + partition - 1) / partition > 128) partition <<= 1;
-    int splits = (max_context_len + partition - 1) / partition;
-    return DecodePlan{partition, splits < 1 ? 1 : splits};
-}
-
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -94,6 +79,41 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
     w.o = align_up(w.ml + units * max_splits * group * sizeof(float2), 256);
     w.total = align_up(w.o + units * max_splits * group * head_dim * sizeof(float), 256);
     return w;
+}
+
+// Items per SM below which decode partitions shrink from 512 to 256 and 128
+// tokens (build-time knob; 0, the measured best, keeps 512 whenever the grid
+// covers two waves: shorter items spend more of their time in the epilogue).
+#ifndef PA_DECODE_ITEMS_PER_SM
+#define PA_DECODE_ITEMS_PER_SM 0
+#endif
+
+DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
+                       int num_sms, size_t workspace_cap) {
+    // Work items are (sequence, partition, kv head).  512-token partitions
+    // keep each item's stream of K/V long; shrink them while the batch would
+    // give fewer than PA_DECODE_ITEMS_PER_SM items per SM (if set) and while
+    // the grid would not cover two waves of the GPU; grow them so
+    // that no (sequence, head) has more than 128 partials to merge and the
+    // split-KV scratch fits `workspace_cap`.  The estimate uses the maximum
+    // context for every sequence: the lengths themselves live on the device.
+    auto items = [&](int part) {
+        long long splits = ((long long)max_context_len + part - 1) / part;
+        return (long long)num_seqs * num_kv_heads * (splits < 1 ? 1 : splits);
+    };
+    int partition = 512;
+    while (partition > 128 && items(partition) < (long long)PA_DECODE_ITEMS_PER_SM * num_sms) partition >>= 1;
+    while (partition > 64 && items(partition) < 2LL * num_sms) partition >>= 1;
+    auto splits_of = [&](int part) {
+        int sp = (int)(((long long)max_context_len + part - 1) / part);
+        return sp < 1 ? 1 : sp;
+    };
+    while (splits_of(partition) > 128 && partition < (1 << 29)) partition <<= 1;
+    while (splits_of(partition) > 1 && partition < (1 << 29) &&
+           decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, splits_of(partition)).total >
+               workspace_cap)
+        partition <<= 1;
+    return DecodePlan{partition, splits_of(partition)};
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -183,7 +203,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
         return 0;
     int num_sms = 0;
     if (check_device(&num_sms) != PA_OK) return 0;
-    DecodePlan plan = plan_decode(num_seqs, num_kv_heads, max_context_len, num_sms);
+    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
     return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total;
 }
 
@@ -201,7 +221,7 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
         return PA_ERR_INVALID_ARG;
     int num_sms = 0;
     if ((rc = check_device(&num_sms)) != PA_OK) return rc;
-    DecodePlan plan = plan_decode(num_seqs, num_kv_heads, max_context_len, num_sms);
+    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
     DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PA_ERR_WORKSPACE;

@@ -26,7 +26,9 @@ struct DecodePlan {
     int partition;   // tokens per split (multiple of 64)
     int max_splits;  // ceil(max_context_len / partition)
 };
-DecodePlan plan_decode(int num_seqs, int num_kv_heads, int max_context_len, int num_sms);
+// `workspace_cap`: largest split-KV scratch the caller can offer (SIZE_MAX: any).
+DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
+                       int num_sms, size_t workspace_cap);
 
 // Workspace layout of pa_decode (byte offsets from the 256-aligned base).
 struct DecodeWorkspace {

@@ -51,6 +51,7 @@ constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | row exchange (6 colu
 constexpr uint32_t kTmemXchg = 384;        // [tile parity][half] partial maxima, then [half] partial sums
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
+
 // shared memory layout (offsets from a 1024-aligned base)
 constexpr int kQ = 0;
 constexpr int kK = kQ + kTileBytes;      // 2 stages
@@ -373,12 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* p_buf = p_tile + (j & 1) * kTileBytes;
             float lsum = 0.f;
             const float neg_m = -m_run;
-            if (dense) {  // half the exponentials on the MUFU unit, half on the FMA pipe
+            if (dense) {
 #pragma unroll
-                for (int k = 0; k < 64; k += 2) {
-                    sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
-                    sv[k + 1] = poly_exp2(fmaf(sv[k + 1], sl2, neg_m));
-                }
+                for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
             } else {
 #pragma unroll
                 for (int k = 0; k < 64; ++k)

@@ -18,6 +18,10 @@ namespace pa {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
                     int head_dim);
+// The same pool as a 3-D map whose box {64, B, D/64} is one block's B rows of
+// one kv head, both 64-column halves ([half][row][64] in shared memory).
+int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
+                         int head_dim);
 
 constexpr uint32_t kSpinLimit = 1u << 18;
 
@@ -236,20 +240,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for finite x in [-126, 64): x = n + f with n = floor(x),
-// f in [0, 1); 2^f from a degree-3 polynomial whose coefficients come from a
-// Remez exchange fit of the relative error on [0, 1) (max relative error
-// 7.5e-5, far inside bf16 rounding); 2^n added to the exponent field.  Lets
-// the softmax split its exponentials between this pipe and the MUFU unit.
-__device__ __forceinline__ float poly_exp2(float x) {
-    x = fmaxf(x, -126.f);
-    const float n = floorf(x);
-    const float f = x - n;
-    float p = fmaf(fmaf(fmaf(0.07802452268953326f, f, 0.22606715539708871f), f, 0.6958335404792924f), f,
-                   0.9999252185659143f);
-    return __int_as_float(__float_as_int(p) + (__float2int_rn(n) << 23));
 }
 
 // Pack two floats into a bf16x2 word (round to nearest even), lo in the low half.

@@ -13,6 +13,34 @@ from . import pa
 from .workloads import Workload
 
 
+# Per-step inputs, in the order they sit in the packed input buffer, and outputs.
+STEP_INPUTS = ("q_decode", "k_new", "v_new", "block_tables", "context_lens", "seq_idx", "pos", "q_prefill",
+               "cu_q_lens", "q_start_pos", "seq_of_chunk")
+STEP_OUTPUTS = ("out_decode", "out_prefill")
+_ALIGN = 256
+
+
+def _packed(tensors, device):
+    """One uint8 buffer holding every tensor at a 256-byte aligned offset, and
+    views of it with each tensor's dtype and shape."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // _ALIGN) * _ALIGN
+    buf = torch.empty(max(total, _ALIGN), dtype=torch.uint8, device=device)
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return buf, views
+
+
+def _packed_views(buf, like):
+    """Views of an existing packed buffer laid out like `_packed` lays out `like`."""
+    offs, total = [], 0
+    for t in like:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // _ALIGN) * _ALIGN
+    return buf, [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, like)]
+
+
 class DeviceStep:
     def __init__(self, w: Workload, device: str | torch.device = "cuda", with_error_count: bool = True):
         dev = torch.device(device)
@@ -21,20 +49,18 @@ class DeviceStep:
         up = lambda t: t.to(dev).contiguous()  # noqa: E731
         self.k_cache = up(w.k_cache)
         self.v_cache = up(w.v_cache)
-        self.block_tables = up(w.block_tables)
-        self.context_lens = up(w.context_lens)
-        self.seq_idx = up(w.seq_idx)
-        self.pos = up(w.pos)
-        self.k_new = up(w.k_new)
-        self.v_new = up(w.v_new)
-        self.q_decode = up(w.q_decode)
-        self.cu_q_lens = up(w.cu_q_lens)
-        self.q_start_pos = up(w.q_start_pos)
-        self.seq_of_chunk = up(w.seq_of_chunk)
-        self.q_prefill = up(w.q_prefill)
+        # The per-step inputs live in one device buffer (and the outputs in
+        # another), so that a serving loop moves a step's inputs in with one
+        # host-to-device copy and its outputs out with one copy back.
+        host_in = [getattr(w, name).contiguous() for name in STEP_INPUTS]
+        self.inbuf, views = _packed(host_in, dev)
+        for name, v, t in zip(STEP_INPUTS, views, host_in):
+            v.copy_(t)
+            setattr(self, name, v)
+        self.outbuf, views = _packed([w.q_decode, w.q_prefill], dev)
+        for name, v in zip(STEP_OUTPUTS, views):
+            setattr(self, name, v)
         self.slots = torch.empty(w.seq_idx.numel(), dtype=torch.int64, device=dev)
-        self.out_decode = torch.empty_like(self.q_decode)
-        self.out_prefill = torch.empty_like(self.q_prefill)
         self.error_count = torch.zeros(1, dtype=torch.int32, device=dev) if with_error_count else None
         self.max_context_len = w.max_decode_context
         nd = w.num_decode
@@ -99,6 +125,38 @@ class DeviceStep:
         """Replay the captured step on the current stream."""
         self.graph.replay()
         return self.out_decode, self.out_prefill
+
+    # serving from host memory ------------------------------------------
+    def pinned_inputs(self) -> torch.Tensor:
+        """A pinned host copy of the packed input buffer (this step's inputs); a
+        serving loop writes each step's inputs into it in the same layout."""
+        return self.inbuf.cpu().pin_memory()
+
+    def pinned_outputs(self) -> torch.Tensor:
+        """A pinned host buffer the size of the packed output buffer."""
+        return torch.empty(self.outbuf.shape, dtype=torch.uint8).pin_memory()
+
+    def input_views(self, host_in: torch.Tensor) -> dict:
+        """Name -> view of a packed input buffer (for filling the next step's inputs)."""
+        _, views = _packed_views(host_in, [getattr(self, n) for n in STEP_INPUTS])
+        return dict(zip(STEP_INPUTS, views))
+
+    def output_views(self, host_out: torch.Tensor):
+        """(decode output, prefill output) as views of a packed output buffer."""
+        _, views = _packed_views(host_out, [self.out_decode, self.out_prefill])
+        return views
+
+    def run_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor, graph: bool = True):
+        """One step from pinned host memory: copy the packed inputs in, run the
+        step (the captured graph when there is one and `graph`), copy the
+        packed outputs back.  Asynchronous on the current stream."""
+        self.inbuf.copy_(host_in, non_blocking=True)
+        if graph and getattr(self, "graph", None) is not None:
+            self.graph.replay()
+        else:
+            self.run()
+        host_out.copy_(self.outbuf, non_blocking=True)
+        return host_out
 
     def errors(self) -> int:
         return int(self.error_count.item()) if self.error_count is not None else 0
