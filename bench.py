@@ -11,9 +11,9 @@ bf16, random non-contiguous block tables.
 Prints ONE JSON line (rank 0).  ``value`` is decode tokens/s (one token per
 sequence per step) over all ranks, timed over exactly K steps, each a replay
 of the step captured as a CUDA graph (``--no-graph``: eager launches).  The
-roofline object describes the decode kernel (algorithmic K/V bytes per launch
-/ its CUDA-event time over eager launches, against the measured HBM copy
-bandwidth).  ``e2e`` re-times the step through the public API from host
+roofline object describes the pa_decode call — the decode kernel and its
+split-KV merge kernel — (algorithmic K/V bytes per call / its CUDA-event
+time over eager launches, against the measured HBM copy bandwidth).  ``e2e`` re-times the step through the public API from host
 memory: the step's packed inputs copied in from pinned memory (one copy), the
 step (graph replay unless ``--no-graph``), the packed outputs copied back (one
 copy), all inside the events.
@@ -155,12 +155,35 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(window), "window": scope}
 
 
-def decode_algorithmic_bytes(w) -> int:
-    """Bytes the decode kernel must move: K and V of every valid context token,
-    the queries and outputs, the block-table entries in use and the lengths."""
+def decode_kv_tokens(w):
+    """(unique, logical) K/V token slots the decode step reads: logical counts
+    every sequence's whole context; unique counts each physical slot once (a
+    block shared by several sequences is read once by an ideal kernel)."""
+    import numpy as np
+
+    nd, B = w.num_decode, w.block_size
+    ctx = np.asarray(w.context_lens[:nd], dtype=np.int64)
+    tables = np.asarray(w.block_tables[:nd], dtype=np.int64)
+    filled = {}  # physical block -> valid slots [0, n) read by some sequence
+    for s in range(nd):
+        L = int(ctx[s])
+        nb = -(-L // B)
+        for b in range(nb):
+            pb = int(tables[s, b])
+            n = min(B, L - b * B)
+            if filled.get(pb, 0) < n:
+                filled[pb] = n
+    return sum(filled.values()), int(ctx.sum())
+
+
+def decode_algorithmic_bytes(w, unique: bool = True) -> int:
+    """Bytes the decode kernel must move: K and V of every valid context token
+    (each physical slot once when `unique`), the queries and outputs, the
+    block-table entries in use and the lengths."""
     nd = w.num_decode
     ctx = [int(x) for x in w.context_lens[:nd]]
-    kv = sum(ctx) * w.kv_bytes_per_token()
+    uniq, logical = decode_kv_tokens(w)
+    kv = (uniq if unique else logical) * w.kv_bytes_per_token()
     qo = 2 * nd * w.num_q_heads * w.head_dim * w.elem_bytes
     tables = sum(-(-L // w.block_size) for L in ctx) * 4 + nd * 4
     return kv + qo + tables
@@ -281,7 +304,12 @@ def run_native(args):
     step = DeviceStep(w, dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    launches_per_step = 2 + (1 if w.num_decode else 0) + (1 if w.num_chunks else 0)
+    decode_launches = 0
+    if w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
+        _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                      step.max_context_len)
+        decode_launches = 1 + (1 if splits > 1 else 0)
+    launches_per_step = 2 + decode_launches + (1 if w.num_chunks else 0)
 
     def barrier():
         if world > 1:
@@ -362,7 +390,8 @@ def run_native(args):
         [statistics.mean(step_ms), statistics.mean(decode_ms), statistics.mean(e2e_ms)], device=dev)
 
     hbm, bf16_tf, bf16_tf_sus, peak_kind = peaks()
-    alg_bytes = decode_algorithmic_bytes(w)
+    alg_bytes = decode_algorithmic_bytes(w)  # each physical K/V slot once
+    logical_bytes = decode_algorithmic_bytes(w, unique=False)  # every sequence's whole context
     achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
     tokens = sharding.total_units(w.num_decode)
     value = tokens / (mean_step * 1e-3)
@@ -373,9 +402,12 @@ def run_native(args):
         "config": workload_config(w),
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "pa_decode", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_tc_kernel + decode_merge_kernel)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "algorithmic_bytes_per_launch": alg_bytes, "ms_per_launch": mean_dec,
+                     "logical_bytes_per_launch": logical_bytes,
+                     "effective_gbs": logical_bytes / (mean_dec * 1e-3) / 1e9,
                      "traffic": recorded_traffic("pa_decode", w.name)},
         "stage_ms": {"slot_mapping+write_kv": statistics.mean(write_ms), "decode": mean_dec,
                      "prefill": statistics.mean(prefill_ms)},

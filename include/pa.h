@@ -114,11 +114,22 @@ PA_API int pa_write_kv(const void* k_new, const void* v_new, int num_tokens, int
 
 /*
  * Bytes of workspace pa_decode needs for these sizes (split-KV partial
- * results plus one ticket counter per (sequence, kv head)).  Deterministic:
+ * results plus two work-queue counters).  Deterministic:
  * the same arguments on the same device always give the same size.
  */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_context_len);
+
+/*
+ * The split-KV plan pa_decode uses for these sizes: *partition receives the
+ * partition length in tokens (a multiple of 64) and *max_splits the number of
+ * partitions of a max_context_len context (1: no merge kernel is launched).
+ * Returns PA_OK, PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED for sizes pa_decode
+ * rejects, or PA_ERR_UNSUPPORTED_DEVICE without a compute capability 10.3
+ * device.  Either output pointer may be NULL.
+ */
+PA_API int pa_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int max_context_len, int* partition, int* max_splits);
 
 /*
  * Paged decode attention, one query token per sequence ([P2] 三、算法流程与
@@ -133,7 +144,8 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv
  *                 and <= max_blocks_per_seq*B (larger entries are clamped and
  *                 counted as errors; pass error_count to see them)
  * Long contexts are split into partitions processed in parallel and merged
- * with a log-sum-exp combine in a fixed order (deterministic).  workspace must
+ * with a log-sum-exp combine in a fixed order (deterministic) by a second
+ * kernel on the same stream.  workspace must
  * hold pa_decode_workspace_size(...) bytes, be 256-byte aligned, and be zeroed
  * once before its first use; the library leaves it zeroed-for-reuse after
  * every call.  One workspace must not serve two calls that may overlap on the
@@ -159,13 +171,15 @@ PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, in
  * memory owned by the library, which every GPU that loads the library keeps
  * until the process exits.  It allocates nothing (no cudaMalloc / cudaFree,
  * no allocating library routine).
- *  - Sizes whose pa_decode_workspace_size(...) exceeds 16 MiB are rejected
- *    with PA_ERR_WORKSPACE before anything is launched.
+ *  - The partitions are made longer (fewer partials) where that keeps the
+ *    scratch within 16 MiB; sizes whose scratch exceeds 16 MiB even with a
+ *    single partition are rejected with PA_ERR_WORKSPACE before anything is
+ *    launched.
  *  - The first call on a device looks up the array's device address on that
  *    device (cudaGetSymbolAddress) and caches it; make that first call before
  *    any stream capture on the device.
  *  - The array is shared by every call and keeps the last call's contents;
- *    each call clears its ticket counters (an asynchronous memset on
+ *    each call clears its work-queue counters (an asynchronous memset on
  *    `stream`) before launching.  Calls that may overlap on the GPU (other
  *    streams, other host threads) race on the array: serialise them.
  */

@@ -5,7 +5,7 @@
 // One CTA per (sequence, kv head, partition): it attends the G query heads of
 // its kv head over its partition's tokens (fma_attend.cuh), then either
 // writes the output (single partition) or stores its partial softmax state
-// and joins the ticketed cross-partition merge (decode_common.cuh).
+// for the split-KV merge (decode_merge.cu).
 #include "decode_common.cuh"
 #include "fma_attend.cuh"
 
@@ -55,7 +55,6 @@ __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(DecodeParams p)
     }
     if (threadIdx.x < G)
         p.ws_ml[(unit * p.max_splits + split) * G + threadIdx.x] = make_float2(m_s[threadIdx.x], l_s[threadIdx.x]);
-    decode_merge_if_last<T>(p, s, kvh, nsplit, S::w_s(smem));
 }
 
 template <typename T, int D>

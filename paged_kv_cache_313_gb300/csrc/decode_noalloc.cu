@@ -4,7 +4,7 @@
 // host runtime with a fixed memory budget that forbids allocation after
 // start-up, a plugin inside another framework's allocator, or code that runs
 // where allocation would synchronise the device.  For them this entry point
-// takes its split-KV scratch (partials and ticket counters) from a fixed
+// takes its split-KV scratch (partials and work-queue counters) from a fixed
 // array in device global memory that belongs to the library itself.
 //
 // The array is file-scope and of fixed size (kNoAllocScratchBytes); every GPU
@@ -73,8 +73,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     if ((rc = scratch_address(&scratch)) != PA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(scratch);
-    // The array keeps the previous call's contents: the ticket counters must start at zero.
-    cudaError_t e = cudaMemsetAsync(ws + lay.counters, 0, lay.ml - lay.counters, st);
+    // The array keeps the previous call's contents: the work-queue counters must start at zero.
+    cudaError_t e = cudaMemsetAsync(ws + lay.work, 0, 2 * sizeof(int), st);
     if (e != cudaSuccess) return set_cuda_error(e);
     DecodeParams p;
     p.out = out;
@@ -84,8 +84,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.error_count = error_count;
-    p.counters = reinterpret_cast<int*>(ws + lay.counters);
-    p.work = p.counters + (size_t)num_seqs * num_kv_heads;
+    p.work = reinterpret_cast<int*>(ws + lay.work);
     p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
     p.ws_o = reinterpret_cast<float*>(ws + lay.o);
     p.num_seqs = num_seqs;
@@ -100,6 +99,5 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     p.partition = plan.partition;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, num_sms, st);
-    return launch_decode_fma(p, dtype, st);
+    return run_decode(p, dtype, num_sms, st);
 }

@@ -11,8 +11,10 @@
 // kv head); partitions are `partition` tokens (a multiple of 64).  Items are
 // numbered densely, sequence-major then partition then kv head, from a
 // prefix sum of the per-sequence item counts that every CTA computes once
-// from context_lens.  One CTA per SM takes items from a global counter in
-// the workspace, so long and short sequences balance dynamically.
+// from context_lens.  Two CTAs per SM take items from a global counter in
+// the workspace, so long and short sequences balance dynamically.  (Putting
+// every sequence's short last partition at the end of the queue was
+// measured 2% slower.)
 //
 // Inside a CTA:
 //  * Warp 4 is the producer.  It walks its items and, for each 64-token
@@ -34,10 +36,11 @@
 //  * Tokens past the context or in blocks with an invalid table entry are
 //    masked (score -inf) and their V rows zeroed before the PV MMA, so stale
 //    or non-finite pool contents never reach the output.
-//  * On an item's last stage the consumers merge their four states in shared
-//    memory and write the output (one partition) or a partial plus a ticket;
-//    the ticket holder merges the partials (decode_common.cuh).  The producer
-//    keeps filling the ring meanwhile.
+//  * On an item's last stage the consumers combine their four states through
+//    slabs in the K tile of the stage just consumed and write the output (one
+//    partition) or a partial for the split-KV merge kernel (decode_merge.cu);
+//    no fence, ticket or wait on other CTAs.  The producer keeps filling the
+//    other stages of the ring meanwhile.
 // Every mbarrier wait is bounded; a timeout counts an error and the kernel
 // still terminates.  The work counter is reset by the last CTA to finish.
 #include "decode_common.cuh"
@@ -76,12 +79,7 @@ struct TcCfg {
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kRing = 0;
     static constexpr int kQ = kRing + kStages * kStageBytes;
-    // [head][D] float: the consumer warps' outputs are summed into it one warp at a time; the
-    // merge weights [head][max_splits <= 128] reuse it afterwards
-    static constexpr int kOred = kQ + kStages * kQBytes;
-    static constexpr int kWmerge = kOred;
-    static constexpr int kOredBytes = (8 * D > 8 * 128 ? 8 * D : 8 * 128) * 4;
-    static constexpr int kCum = kOred + kOredBytes;                     // int [kMaxSeqs + 1]
+    static constexpr int kCum = kQ + kStages * kQBytes;  // int [kMaxSeqs + 1]
     static constexpr int kInfo = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
     static constexpr int kEnd = kBars + 2 * kStages * 8;
@@ -108,9 +106,10 @@ struct ConsumerBarrier {
     __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 };
 
-// Item -> (sequence, partition, kv head) through the prefix sum cum[0..N].
+// Item -> (sequence, partition, kv head) through the prefix sum cum[0..N] of
+// the per-sequence item counts: the largest s with cum[s] <= item.
 __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int item, int& s, int& split, int& kvh) {
-    int lo = 0, hi = N - 1;  // largest s with cum[s] <= item
+    int lo = 0, hi = N - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
         if (cum[mid] <= item) lo = mid; else hi = mid - 1;
@@ -135,12 +134,13 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + C::kInfo);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBars);
     uint64_t* empty = full + C::kStages;
-    __shared__ float red_m[C::kConsumerWarps][8], red_l[C::kConsumerWarps][8];
+    __shared__ float red_m[2][C::kConsumerWarps][8], red_l[2][C::kConsumerWarps][8];
     __shared__ int warp_tot[C::kThreads / 32];
-    __shared__ int s_flag;
     __shared__ int s_total;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
 
     // ---- per-sequence item counts and their exclusive prefix sum (every CTA, once)
     {
@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         }
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*c4 and 2*c4+1
         const float sl2 = p.scale_log2;
+        int item_parity = 0;
         const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kHalves * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
             const int slot = stage_no % C::kStages;
@@ -399,11 +400,20 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 if (rows != 0xFFFFu) fence_proxy_async_smem();  // zeroing before the slot's next TMA write
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (!(inf.flags & 2)) continue;
+            if (!(inf.flags & 2)) {
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                continue;
+            }
 
             // ---------------------------------------------------- item epilogue
+            // The four warps' states are combined through four [head][D] fp32
+            // slabs in the K tile of the stage just consumed; the stage goes
+            // back to the producer only after that.  The (m, l) exchange
+            // arrays alternate between items so that a warp running ahead
+            // into the next epilogue never overwrites values still being read.
             const ConsumerBarrier bar;
+            const int par = item_parity;
+            item_parity ^= 1;
             float L0 = l0, L1 = l1;
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -411,84 +421,62 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 L1 += __shfl_xor_sync(0xffffffffu, L1, off);
             }
             if (g4 == 0) {
-                red_m[warp][2 * c4] = m0;
-                red_m[warp][2 * c4 + 1] = m1;
-                red_l[warp][2 * c4] = L0;
-                red_l[warp][2 * c4 + 1] = L1;
+                red_m[par][warp][2 * c4] = m0;
+                red_m[par][warp][2 * c4 + 1] = m1;
+                red_l[par][warp][2 * c4] = L0;
+                red_l[par][warp][2 * c4 + 1] = L1;
             }
-            bar();
+            bar();  // every warp is done with this stage's K/V, and the states are visible
             float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::kConsumerWarps; ++w) {
-                M0 = fmaxf(M0, red_m[w][2 * c4]);
-                M1 = fmaxf(M1, red_m[w][2 * c4 + 1]);
+                M0 = fmaxf(M0, red_m[par][w][2 * c4]);
+                M1 = fmaxf(M1, red_m[par][w][2 * c4 + 1]);
             }
             const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M0);
             const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M1);
+            float* slabs = reinterpret_cast<float*>(smem + C::kRing + slot * C::kStageBytes);  // [warp][head][D]
+            {
+                float* my = slabs + warp * 8 * D;
 #pragma unroll
-            for (int mt = 0; mt < KT; ++mt) {
-                o[mt][0] *= f0;
-                o[mt][1] *= f1;
-                o[mt][2] *= f0;
-                o[mt][3] *= f1;
-            }
-            // sum the four warps' O^T through one [head][D] slab: warp 3 -> 2 -> 1 -> 0 -> slab
-            float* ored = reinterpret_cast<float*>(smem + C::kOred);
-            for (int w = C::kConsumerWarps - 1; w >= 0; --w) {
-                if (warp == w) {
-#pragma unroll
-                    for (int mt = 0; mt < KT; ++mt) {
-                        const int d = mt * 16 + g4;
-                        ored[(2 * c4) * D + d] = o[mt][0];
-                        ored[(2 * c4 + 1) * D + d] = o[mt][1];
-                        ored[(2 * c4) * D + d + 8] = o[mt][2];
-                        ored[(2 * c4 + 1) * D + d + 8] = o[mt][3];
-                    }
+                for (int mt = 0; mt < KT; ++mt) {
+                    const int d = mt * 16 + g4;
+                    my[(2 * c4) * D + d] = o[mt][0] * f0;
+                    my[(2 * c4 + 1) * D + d] = o[mt][1] * f1;
+                    my[(2 * c4) * D + d + 8] = o[mt][2] * f0;
+                    my[(2 * c4 + 1) * D + d + 8] = o[mt][3] * f1;
                 }
-                bar();
-                if (w == 0) break;
-                if (warp == w - 1) {
-#pragma unroll
-                    for (int mt = 0; mt < KT; ++mt) {
-                        const int d = mt * 16 + g4;
-                        o[mt][0] += ored[(2 * c4) * D + d];
-                        o[mt][1] += ored[(2 * c4 + 1) * D + d];
-                        o[mt][2] += ored[(2 * c4) * D + d + 8];
-                        o[mt][3] += ored[(2 * c4 + 1) * D + d + 8];
-                    }
-                }
-                bar();
             }
+            fence_proxy_async_smem();  // these writes precede the slot's next TMA write
+            bar();
             const size_t unit = decode_unit(p, inf.s, inf.kvh);
             __nv_bfloat16* out =
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;
             float* wo = p.ws_o + (unit * p.max_splits + inf.split) * G * D;
             for (int idx = tid; idx < G * D; idx += 32 * C::kConsumerWarps) {
-                const int h = idx / D, d = idx % D;
+                const int h = idx / D;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[w][h]);
+                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[par][w][h]);
                 float Ls = 0.f;
 #pragma unroll
                 for (int w = 0; w < C::kConsumerWarps; ++w) {
-                    const float mw = red_m[w][h];
-                    if (mw != -INFINITY) Ls += red_l[w][h] * fast_exp2(mw - M);
+                    const float mw = red_m[par][w][h];
+                    if (mw != -INFINITY) Ls += red_l[par][w][h] * fast_exp2(mw - M);
                 }
-                const float acc = ored[h * D + d];
+                float acc = slabs[idx];
+#pragma unroll
+                for (int w = 1; w < C::kConsumerWarps; ++w) acc += slabs[w * 8 * D + idx];
                 const float val = Ls > 0.f ? acc / Ls : 0.f;
                 if (inf.nsplit == 1) {
                     out[idx] = __float2bfloat16_rn(val);
                 } else {
                     wo[idx] = val;
-                    if (d == 0) p.ws_ml[(unit * p.max_splits + inf.split) * G + h] = make_float2(M, Ls);
+                    if (idx % D == 0) p.ws_ml[(unit * p.max_splits + inf.split) * G + h] = make_float2(M, Ls);
                 }
             }
-            if (inf.nsplit > 1)
-                decode_ticket_merge<__nv_bfloat16>(p, inf.s, inf.kvh, inf.nsplit,
-                                                   reinterpret_cast<float*>(smem + C::kWmerge), &s_flag, tid,
-                                                   32 * C::kConsumerWarps, bar);
-            else
-                bar();  // red_m / ored free for the next item
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);  // this warp has read the slabs
         }
     }
 
@@ -516,8 +504,8 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * PA_DECODE_CTAS_PER_SM;
     int grid = (int)(max_items < slots ? max_items : slots);
-    decode_tc_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tmk, tmv, p, p.work);
-    return check_launch();
+    return launch_kernel(decode_tc_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv, p,
+                         p.work);
 }
 
 }  // namespace

@@ -24,14 +24,13 @@ template <int D>
 struct FmaShape {
     static constexpr int kItems = kFmaMaxGroup * D / kFmaThreads;  // (g, d) outputs per thread (upper bound)
     static constexpr int kPerLane = D / 32;
-    // dynamic shared memory: q [16][D], p [16][kSub], w [16][128], blocks [kSub+1]
+    // dynamic shared memory: q [16][D], p [16][kSub], blocks [kSub+1]
     static constexpr size_t kSmemBytes =
-        sizeof(float) * (kFmaMaxGroup * D + kFmaMaxGroup * kFmaSub + kFmaMaxGroup * 128) + sizeof(int) * (kFmaSub + 1);
+        sizeof(float) * (kFmaMaxGroup * D + kFmaMaxGroup * kFmaSub) + sizeof(int) * (kFmaSub + 1);
     __device__ static float* q_s(float* smem) { return smem; }
     __device__ static float* p_s(float* smem) { return smem + kFmaMaxGroup * D; }
-    __device__ static float* w_s(float* smem) { return smem + kFmaMaxGroup * D + kFmaMaxGroup * kFmaSub; }
     __device__ static int* blk_s(float* smem) {
-        return reinterpret_cast<int*>(smem + kFmaMaxGroup * D + kFmaMaxGroup * kFmaSub + kFmaMaxGroup * 128);
+        return reinterpret_cast<int*>(smem + kFmaMaxGroup * D + kFmaMaxGroup * kFmaSub);
     }
 };
 

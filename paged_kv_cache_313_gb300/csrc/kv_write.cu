@@ -19,6 +19,8 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, in
                                     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos,
                                     int num_tokens, int block_size, int num_blocks, int64_t* __restrict__ slots,
                                     int32_t* error_count) {
+    pdl_trigger();
+    pdl_wait();
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens) return;
     int p = pos[t];
@@ -43,6 +45,8 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, in
 __global__ void write_kv_kernel(const int4* __restrict__ k_new, const int4* __restrict__ v_new, int row_vecs,
                                 int4* __restrict__ k_cache, int4* __restrict__ v_cache, long long num_slots,
                                 const int64_t* __restrict__ slots, int32_t* error_count) {
+    pdl_trigger();
+    pdl_wait();
     int t = blockIdx.x;
     long long slot = slots[t];
     if (slot < 0) return;
@@ -91,10 +95,9 @@ int launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_block
                         const int32_t* pos, int num_tokens, int block_size, int num_blocks, int64_t* slot_mapping,
                         int32_t* error_count, cudaStream_t stream) {
     const int threads = 256;
-    slot_mapping_kernel<<<(num_tokens + threads - 1) / threads, threads, 0, stream>>>(
-        block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, num_tokens, block_size, num_blocks, slot_mapping,
-        error_count);
-    return check_launch();
+    return launch_kernel(slot_mapping_kernel, dim3((num_tokens + threads - 1) / threads), dim3(threads), 0, stream,
+                         block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, num_tokens, block_size,
+                         num_blocks, slot_mapping, error_count);
 }
 
 int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
@@ -102,10 +105,10 @@ int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int ro
                     cudaStream_t stream) {
     int row_vecs = row_bytes / 16;
     int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
-    write_kv_kernel<<<num_tokens, threads, 0, stream>>>(
-        static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs, static_cast<int4*>(k_cache),
-        static_cast<int4*>(v_cache), num_slots, slot_mapping, error_count);
-    return check_launch();
+    return launch_kernel(write_kv_kernel, dim3(num_tokens), dim3(threads), 0, stream,
+                         static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs,
+                         static_cast<int4*>(k_cache), static_cast<int4*>(v_cache), num_slots, slot_mapping,
+                         error_count);
 }
 
 int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,

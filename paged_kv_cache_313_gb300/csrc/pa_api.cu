@@ -74,8 +74,8 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
     DecodeWorkspace w;
     size_t units = (size_t)num_seqs * num_kv_heads;
     size_t group = (size_t)(num_q_heads / num_kv_heads);
-    w.counters = 0;
-    w.ml = align_up((units + 2) * sizeof(int), 256);
+    w.work = 0;
+    w.ml = 256;
     w.o = align_up(w.ml + units * max_splits * group * sizeof(float2), 256);
     w.total = align_up(w.o + units * max_splits * group * head_dim * sizeof(float), 256);
     return w;
@@ -114,6 +114,12 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
                workspace_cap)
         partition <<= 1;
     return DecodePlan{partition, splits_of(partition)};
+}
+
+int run_decode(const DecodeParams& p, int dtype, int num_sms, cudaStream_t stream) {
+    int rc = decode_tc_supported(p, dtype) ? launch_decode_tc(p, num_sms, stream) : launch_decode_fma(p, dtype, stream);
+    if (rc != PA_OK) return rc;
+    return launch_decode_merge(p, dtype, num_sms, stream);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -207,6 +213,19 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total;
 }
 
+int pa_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                   int max_context_len, int* partition, int* max_splits) {
+    if (num_seqs < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PA_OK) return rc;
+    int num_sms = 0;
+    if ((rc = check_device(&num_sms)) != PA_OK) return rc;
+    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
+    if (partition) *partition = plan.partition;
+    if (max_splits) *max_splits = plan.max_splits;
+    return PA_OK;
+}
+
 int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int dtype,
               const void* k_cache, const void* v_cache, int num_blocks, int block_size,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
@@ -234,8 +253,7 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.error_count = error_count;
-    p.counters = reinterpret_cast<int*>(ws + lay.counters);
-    p.work = p.counters + (size_t)num_seqs * num_kv_heads;
+    p.work = reinterpret_cast<int*>(ws + lay.work);
     p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
     p.ws_o = reinterpret_cast<float*>(ws + lay.o);
     p.num_seqs = num_seqs;
@@ -250,8 +268,7 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
     p.partition = plan.partition;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
-    if (decode_tc_supported(p, dtype)) return launch_decode_tc(p, num_sms, static_cast<cudaStream_t>(stream));
-    return launch_decode_fma(p, dtype, static_cast<cudaStream_t>(stream));
+    return run_decode(p, dtype, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 size_t pa_prefill_workspace_size(int num_chunks, int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,

@@ -19,6 +19,35 @@ int check_device(int* num_sms);     // PA_OK on an sm_103 device (cached per dev
 // device (once per kernel and device).
 int ensure_dynamic_smem(const void* kernel, size_t bytes);
 
+// Programmatic dependent launch.  The hot-path kernels are launched with
+// programmatic stream serialisation, so a kernel's launch and CTA start-up
+// overlap the tail of the kernel before it on the stream.  Every such kernel
+// executes pdl_wait() before its first global-memory access (the wait returns
+// once the preceding grid has completed and its writes are visible, and at
+// once when there is no programmatic predecessor) and pdl_trigger() at its
+// start, which lets the next kernel begin launching.  Build with
+// -DPA_USE_PDL=0 for plain launches.
+#ifndef PA_USE_PDL
+#define PA_USE_PDL 1
+#endif
+
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                  Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PA_USE_PDL ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    return e == cudaSuccess ? PA_OK : set_cuda_error(e);
+}
+
 inline int elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
 // Split-KV partition policy shared by pa_decode and pa_decode_workspace_size.
@@ -32,7 +61,7 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
 
 // Workspace layout of pa_decode (byte offsets from the 256-aligned base).
 struct DecodeWorkspace {
-    size_t counters;  // int32 [num_seqs][num_kv_heads] tickets, then 2 work-queue counters
+    size_t work;      // int32 [2]: the persistent decode kernel's work-queue counters
     size_t ml;        // float2 [num_seqs][num_kv_heads][max_splits][G]  (running max in log2 units, sum)
     size_t o;         // float  [num_seqs][num_kv_heads][max_splits][G][head_dim]
     size_t total;
@@ -48,7 +77,6 @@ struct DecodeParams {
     const int32_t* block_tables;
     const int32_t* context_lens;
     int32_t* error_count;
-    int* counters;      // ticket per (sequence, kv head)
     int* work;          // work[0]: next item, work[1]: finished CTAs (persistent kernel)
     float2* ws_ml;
     float* ws_o;
@@ -89,10 +117,17 @@ int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_s
 int launch_decode_fma(const DecodeParams& p, int dtype, cudaStream_t stream);
 bool decode_tc_supported(const DecodeParams& p, int dtype);
 int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream);
+int launch_decode_merge(const DecodeParams& p, int dtype, int num_sms, cudaStream_t stream);
+// The decode kernel for these parameters (tensor-core or FMA), then the
+// split-KV merge when there is more than one partition.
+int run_decode(const DecodeParams& p, int dtype, int num_sms, cudaStream_t stream);
 bool prefill_tc_supported(const PrefillParams& p, int dtype);
 int launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- device side
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 

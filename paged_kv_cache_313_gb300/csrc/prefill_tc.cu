@@ -90,6 +90,8 @@ struct Bars {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int c = blockIdx.z, kvh = blockIdx.y;
     const int G = p.group, B = p.block_size;
     const int pos_per_tile = kTileQ / G;
@@ -497,8 +499,7 @@ int launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
     if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_tc_kernel), kSmemBytes)) != PA_OK) return rc;
     const int pos_per_tile = kTileQ / p.group;
     dim3 grid((p.max_q_len + pos_per_tile - 1) / pos_per_tile, p.num_kv_heads, p.num_chunks);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmq, tmk, tmv, p);
-    return check_launch();
+    return launch_kernel(prefill_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, tmq, tmk, tmv, p);
 }
 
 }  // namespace pa

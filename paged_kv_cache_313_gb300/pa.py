@@ -19,8 +19,8 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_prefill_workspace_size",
-           "pa_prefill_chunk", "pa_copy_blocks")
+           "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_noalloc",
+           "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_copy_blocks")
 
 
 class PaError(RuntimeError):
@@ -41,6 +41,7 @@ _SIGNATURES = {
     "pa_slot_mapping": ([_p, _i, _i, _p, _p, _i, _i, _i, _p, _p, _p], _i),
     "pa_write_kv": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _p, _p], _i),
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
+    "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
     "pa_decode_noalloc": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p], _i),
     "pa_prefill_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
@@ -136,6 +137,14 @@ def pa_write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, error_count=None, 
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len) -> int:
     return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                               max_context_len))
+
+
+def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len):
+    """(partition length in tokens, number of partitions) pa_decode uses for these sizes."""
+    part, splits = ctypes.c_int(0), ctypes.c_int(0)
+    _check("pa_decode_plan", lib().pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                                  max_context_len, ctypes.byref(part), ctypes.byref(splits)))
+    return part.value, splits.value
 
 
 def new_decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,

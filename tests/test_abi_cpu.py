@@ -58,6 +58,9 @@ def test_host_side_rejections_need_no_device(lib):
     args[3], args[4], args[5] = 3, 2, 128
     assert lib.pa_decode(*args) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode_workspace_size(4, 3, 2, 128, 16, 100) == 0
+    assert lib.pa_decode_plan(-1, 8, 8, 128, 16, 100, None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_plan(4, 3, 2, 128, 16, 100, None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_plan(4, 8, 8, 96, 16, 100, None, None) == pa.PA_ERR_UNSUPPORTED
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 0, None, None) == pa.PA_OK
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 2, None, None) == \
         pa.PA_ERR_INVALID_ARG

@@ -264,3 +264,16 @@ def test_run_from_host_matches_device_step():
     assert not torch.equal(fresh[0], want[0])
     for x, y in zip(fresh, st.output_views(host_out)):
         assert torch.equal(x.cpu(), y)
+
+
+def test_decode_plan_matches_workspace_and_launches():
+    """The plan reported through the ABI is the one pa_decode sizes its
+    workspace for: 512-token partitions on the bf16 decode workload (64
+    sequences, 8 kv heads, contexts up to 4096) and one partition (no merge
+    kernel) for a context that fits one."""
+    part, splits = pa.pa_decode_plan(64, 32, 8, 128, 16, 4096)
+    assert (part, splits) == (512, 8)
+    need = pa.pa_decode_workspace_size(64, 32, 8, 128, 16, 4096)
+    assert need >= 64 * 8 * splits * 4 * 128 * 4
+    part1, splits1 = pa.pa_decode_plan(512, 32, 8, 128, 16, 300)
+    assert splits1 == 1 and part1 >= 300
