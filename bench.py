@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cascade", dest="cascade", action="store_false",
+                    help="plain paged decode even where decode sequences share prefixes")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps eagerly instead of replaying a captured CUDA graph")
     return ap.parse_args()
@@ -281,6 +283,10 @@ def workload_config(w):
            "prefill_chunks": w.num_chunks, "prefill_queries": int(w.cu_q_lens[-1]) if w.num_chunks else 0,
            "new_tokens": int(w.seq_idx.numel()), "seed": w.meta.get("seed", 0),
            "l2": "flushed before every timed step (512 MiB write)"}
+    shared = int((w.prefix_lens > 0).sum()) if w.num_decode else 0
+    if shared:
+        cfg["shared_prefix_seqs"] = shared
+        cfg["groups"] = int(len(w.group_offsets) - 1)
     return cfg
 
 
@@ -301,11 +307,13 @@ def run_native(args):
 
     pa.lib()  # fail loudly if the CUDA library is missing
     w = W.make(args.workload, sharding.shard_seed(args.seed, rank))
-    step = DeviceStep(w, dev)
+    step = DeviceStep(w, dev, cascade=args.cascade)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     decode_launches = 0
-    if w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
+    if step.use_cascade:  # prefix pass, tail pass, merge
+        decode_launches = 3
+    elif w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
         _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                       step.max_context_len)
         decode_launches = 1 + (1 if splits > 1 else 0)
@@ -402,7 +410,10 @@ def run_native(args):
         "config": workload_config(w),
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_tc_kernel + decode_merge_kernel)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("pa_decode_cascade (prefill_tc_kernel prefix pass + decode_tc_kernel tails + "
+                                "decode_merge_kernel)" if step.use_cascade
+                                else "pa_decode (decode_tc_kernel + decode_merge_kernel)"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "algorithmic_bytes_per_launch": alg_bytes, "ms_per_launch": mean_dec,

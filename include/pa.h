@@ -159,6 +159,40 @@ PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, in
               int32_t* error_count, void* stream);
 
 /*
+ * Cascade decode for sequences that share a prefix (parallel sampling, beam
+ * search, a common system prompt): "什么是 PagedAttention？", 共享但不污染状态
+ * (several sequences map the same physical blocks).  Computes exactly what
+ * pa_decode computes, but each group's shared prefix is read from memory once
+ * for all of the group's sequences instead of once per sequence:
+ *   - groups: sequences [group_offsets[g], group_offsets[g+1]) form group g
+ *     (int32 [num_groups+1], non-decreasing, each group a contiguous range of
+ *     sequence indices; sequences outside every group, or in a group of one,
+ *     are plain decode);
+ *   - prefix_lens: int32 [num_seqs], the number of leading context tokens a
+ *     sequence shares with its group (0: none).  All members of a group must
+ *     have the same prefix length and the same K/V for those tokens (the same
+ *     physical blocks, or copy-on-write copies of them); the prefix is read
+ *     through the group's first member's block table, and a member whose
+ *     prefix length differs from the first member's is counted in error_count.
+ *   - max_group_size >= the largest group.
+ * Three kernels run on `stream`: the prefix pass (the group's queries, G per
+ * sequence, stacked as the rows of a tensor-core tile against the prefix's
+ * keys), the tail pass (each sequence's tokens [prefix_len, L)), and the
+ * log-sum-exp merge of the two.  workspace: pa_decode_cascade_workspace_size
+ * bytes, 256-byte aligned, zeroed once.  Supported: bf16, head_dim 128,
+ * num_q_heads/num_kv_heads in {1, 2, 4, 8}, block_size 8..64; otherwise
+ * PA_ERR_UNSUPPORTED (use pa_decode).
+ */
+PA_API size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                               int block_size, int max_context_len);
+PA_API int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads,
+                             int head_dim, int dtype, const void* k_cache, const void* v_cache, int num_blocks,
+                             int block_size, const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int max_context_len, const int32_t* group_offsets,
+                             int num_groups, int max_group_size, const int32_t* prefix_lens, float scale,
+                             void* workspace, size_t workspace_bytes, int32_t* error_count, void* stream);
+
+/*
  * pa_decode for callers that cannot allocate device memory.  The pages have
  * no counterpart: this is a deployment aid, not part of the method.
  *

@@ -28,6 +28,17 @@ __device__ __forceinline__ int decode_context(const DecodeParams& p, int s, bool
     return L;
 }
 
+// Decode range of sequence s (context L): tokens [*prefix, L) where *prefix is
+// the cascade prefix length (0 without one), clamped to [0, L).  Returns the
+// first token of partition 0, *prefix rounded down to a multiple of 64 so that
+// partitions stay block aligned; tokens below *prefix are masked.
+__device__ __forceinline__ int decode_start(const DecodeParams& p, int s, int L, int* prefix) {
+    int pre = p.prefix_lens ? p.prefix_lens[s] : 0;
+    pre = pre < 0 ? 0 : (pre > L ? L : pre);
+    *prefix = pre;
+    return pre & ~63;
+}
+
 __device__ __forceinline__ size_t decode_unit(const DecodeParams& p, int s, int kvh) {
     return (size_t)s * p.num_kv_heads + kvh;
 }

@@ -70,7 +70,7 @@ int launch_fma(const DecodeParams& p, cudaStream_t stream) {
 }  // namespace
 
 int launch_decode_fma(const DecodeParams& p, int dtype, cudaStream_t stream) {
-    if (p.group > kFmaMaxGroup || p.max_splits > 128) return PA_ERR_UNSUPPORTED;
+    if (p.group > kFmaMaxGroup || p.max_splits > 128 || p.prefix_lens != nullptr) return PA_ERR_UNSUPPORTED;
     if (p.num_kv_heads > 65535 || p.max_splits > 65535) return PA_ERR_UNSUPPORTED;
     if (dtype == PA_F32) return p.head_dim == 64 ? launch_fma<float, 64>(p, stream) : launch_fma<float, 128>(p, stream);
     return p.head_dim == 64 ? launch_fma<__nv_bfloat16, 64>(p, stream) : launch_fma<__nv_bfloat16, 128>(p, stream);

@@ -6,7 +6,9 @@
 // combine ("PagedAttention学习笔记", 与 FlashAttention 的关系: the formula is
 // unchanged, only tiled with an online softmax):
 //     m* = max_i m_i,   w_i = l_i 2^(m_i - m*),   out = sum_i w_i o_i / sum_i w_i
-// (partitions with l_i = 0 hold no valid token and get w_i = 0).
+// (partitions with l_i = 0 hold no valid token and get w_i = 0).  In a
+// cascade (pa_decode_cascade) slot 0 holds the shared prefix's partial and the
+// tail's partitions follow it.
 //
 // One warp per (sequence, query head) at a time, grid-stride over all of
 // them (a grid of at most a few CTAs per SM, so sequences with a single
@@ -35,16 +37,19 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     for (long long u = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5); u < units; u += warps) {
         const int s = (int)(u / Hq), h = (int)(u - (long long)s * Hq);
         const int L = decode_context(p, s, false);
-        const int nsplit = num_partitions(L, p.partition);
-        if (nsplit <= 1) continue;  // the decode kernel wrote this output directly
+        int pre;
+        const int nsplit = num_partitions(L - decode_start(p, s, L, &pre), p.partition);
+        if (nsplit <= 1 && pre == 0) continue;  // the decode kernel wrote this output directly
+        // partial slots [0, split_base) hold the cascade prefix (valid when pre > 0), then the partitions
+        const int first = pre > 0 ? 0 : p.split_base, ntot = p.split_base + nsplit;
         const int kvh = h / G, g = h - kvh * G;
-        const size_t base = decode_unit(p, s, kvh) * p.max_splits * G + g;  // (partition 0, head g)
-        // weights w_i = l_i 2^(m_i - m*) / sum: nsplit <= 128, four per lane
+        const size_t base = decode_unit(p, s, kvh) * p.max_splits * G + g;  // (slot 0, head g)
+        // weights w_i = l_i 2^(m_i - m*) / sum: at most 128 slots, four per lane
         float2 v[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int i = lane + 32 * k;
-            v[k] = i < nsplit ? __ldcg(p.ws_ml + base + (size_t)i * G) : make_float2(-INFINITY, 0.f);
+            v[k] = i >= first && i < ntot ? __ldcg(p.ws_ml + base + (size_t)i * G) : make_float2(-INFINITY, 0.f);
         }
         float m = -INFINITY;
 #pragma unroll
@@ -65,11 +70,11 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
         const float4* o = reinterpret_cast<const float4*>(p.ws_o + base * D) + (lane < kLanes ? lane : 0);
         const size_t stride4 = (size_t)G * D / 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i0 = 0; i0 < nsplit; i0 += kMergeUnroll) {
+        for (int i0 = first; i0 < ntot; i0 += kMergeUnroll) {
             float4 x[kMergeUnroll];
 #pragma unroll
             for (int k = 0; k < kMergeUnroll; ++k)
-                if (i0 + k < nsplit) x[k] = __ldcg(o + (size_t)(i0 + k) * stride4);
+                if (i0 + k < ntot) x[k] = __ldcg(o + (size_t)(i0 + k) * stride4);
 #pragma unroll
             for (int k = 0; k < kMergeUnroll; ++k) {
                 const int i = i0 + k;
@@ -77,7 +82,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
                 const int slot = i >> 5;
                 const float wsrc = slot == 0 ? w[0] : slot == 1 ? w[1] : slot == 2 ? w[2] : w[3];
                 const float wi = __shfl_sync(0xffffffffu, wsrc, i & 31);
-                if (i < nsplit) {
+                if (i < ntot) {
                     acc.x = fmaf(wi, x[k].x, acc.x);
                     acc.y = fmaf(wi, x[k].y, acc.y);
                     acc.z = fmaf(wi, x[k].z, acc.z);
@@ -105,7 +110,7 @@ int launch_merge(const DecodeParams& p, int grid, cudaStream_t stream) {
 }  // namespace
 
 int launch_decode_merge(const DecodeParams& p, int dtype, int num_sms, cudaStream_t stream) {
-    if (p.max_splits <= 1) return PA_OK;
+    if (p.max_splits <= 1 && p.prefix_lens == nullptr) return PA_OK;
     if (p.max_splits > 128) return PA_ERR_UNSUPPORTED;
     const long long units = (long long)p.num_seqs * p.num_q_heads;
     const long long want = (units + kMergeThreads / 32 - 1) / (kMergeThreads / 32);

@@ -60,7 +60,7 @@ constexpr int kMaxSeqsPersistent = PA_DECODE_CTAS_PER_SM == 1 ? 2048 : 1024;
 
 struct StageInfo {
     int s, kvh, split, nsplit;
-    int flags;  // bit 0: first stage of its item, bit 1: last stage of its item
+    int flags;  // bit 0: first stage of its item, bit 1: last stage, bit 2: the item writes the output
     int ntok;   // tokens of this stage (0..64)
     unsigned long long valid;  // bit r: token row r holds a valid token
 };
@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         int local = 0;
         for (int i = 0; i < per && first + i < N; ++i) {
             const int L = decode_context(p, first + i, blockIdx.x == 0);
-            local += num_partitions(L, p.partition) * Hkv;
+            int pre;
+            local += num_partitions(L - decode_start(p, first + i, L, &pre), p.partition) * Hkv;
         }
         int incl = local;  // inclusive scan over the warp
 #pragma unroll
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         for (int i = 0; i < per && first + i < N; ++i) {
             cum[first + i] = run;
             const int L = decode_context(p, first + i, false);
-            run += num_partitions(L, p.partition) * Hkv;
+            int pre;
+            run += num_partitions(L - decode_start(p, first + i, L, &pre), p.partition) * Hkv;
         }
         if (threadIdx.x == C::kThreads - 1) {
             int tot = 0;
@@ -200,8 +202,11 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             int s, split, kvh;
             decode_item(cum, N, Hkv, item, s, split, kvh);
             const int L = decode_context(p, s, false);
-            const int nsplit = num_partitions(L, p.partition);
-            const int j0 = split * p.partition;
+            int pre;
+            const int j_first = decode_start(p, s, L, &pre);
+            const int nsplit = num_partitions(L - j_first, p.partition);
+            const bool direct = nsplit == 1 && pre == 0;
+            const int j0 = j_first + split * p.partition;
             const int ntok = max(0, min(L, j0 + p.partition) - j0);
             const int nst = max(1, (ntok + C::kStageTok - 1) / C::kStageTok);
             const int nblk = (ntok + B - 1) / B;
@@ -241,13 +246,15 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                         bytes += 2u * C::kHalves * B * 128u;
                     }
                 }
+                const int skip = pre - (j0 + t0);  // tokens of a cascade prefix at the start of the stage
+                if (skip > 0) valid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
                 if (lane == 0) {
                     StageInfo& inf = info[slot];
                     inf.s = s;
                     inf.kvh = kvh;
                     inf.split = split;
                     inf.nsplit = nsplit;
-                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0);
+                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) | (direct ? 4 : 0);
                     inf.ntok = nt;
                     inf.valid = valid;
                     mbar_arrive_expect_tx(&full[slot], bytes);
@@ -452,7 +459,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             const size_t unit = decode_unit(p, inf.s, inf.kvh);
             __nv_bfloat16* out =
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;
-            float* wo = p.ws_o + (unit * p.max_splits + inf.split) * G * D;
+            const size_t slot_ws = unit * p.max_splits + inf.split + p.split_base;
+            float* wo = p.ws_o + slot_ws * G * D;
             for (int idx = tid; idx < G * D; idx += 32 * C::kConsumerWarps) {
                 const int h = idx / D;
                 float M = -INFINITY;
@@ -468,11 +476,11 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
 #pragma unroll
                 for (int w = 1; w < C::kConsumerWarps; ++w) acc += slabs[w * 8 * D + idx];
                 const float val = Ls > 0.f ? acc / Ls : 0.f;
-                if (inf.nsplit == 1) {
+                if (inf.flags & 4) {
                     out[idx] = __float2bfloat16_rn(val);
                 } else {
                     wo[idx] = val;
-                    if (idx % D == 0) p.ws_ml[(unit * p.max_splits + inf.split) * G + h] = make_float2(M, Ls);
+                    if (idx % D == 0) p.ws_ml[slot_ws * G + h] = make_float2(M, Ls);
                 }
             }
             __syncwarp();

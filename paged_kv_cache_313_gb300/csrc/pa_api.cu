@@ -321,4 +321,114 @@ int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const i
     return launch_prefill_fma(p, dtype, static_cast<cudaStream_t>(stream));
 }
 
+// ---- cascade decode: shared prefixes read once per group
+
+// Plan of the cascade: the tail pass uses pa_decode's partitions, and slot 0 of
+// every (sequence, kv head) holds the prefix partial, so max_splits grows by one.
+static DecodePlan plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
+                               int num_sms) {
+    DecodePlan pl = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
+    while (pl.max_splits + 1 > 128) {
+        pl.partition <<= 1;
+        pl.max_splits = (int)(((long long)max_context_len + pl.partition - 1) / pl.partition);
+    }
+    pl.max_splits += 1;
+    return pl;
+}
+
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int block_size, int max_context_len) {
+    if (num_seqs < 0 || max_context_len < 0 || decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size))
+        return 0;
+    int num_sms = 0;
+    if (check_device(&num_sms) != PA_OK) return 0;
+    DecodePlan plan = plan_cascade(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms);
+    return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total;
+}
+
+int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      int dtype, const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                      int max_context_len, const int32_t* group_offsets, int num_groups, int max_group_size,
+                      const int32_t* prefix_lens, float scale, void* workspace, size_t workspace_bytes,
+                      int32_t* error_count, void* stream) {
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0 || num_groups < 0 ||
+        max_group_size < 0)
+        return PA_ERR_INVALID_ARG;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PA_OK) return rc;
+    if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !context_lens || !prefix_lens || !block_tables ||
+        (num_groups > 0 && !group_offsets))
+        return PA_ERR_INVALID_ARG;
+    int num_sms = 0;
+    if ((rc = check_device(&num_sms)) != PA_OK) return rc;
+    DecodePlan plan = plan_cascade(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms);
+    DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.error_count = error_count;
+    p.work = reinterpret_cast<int*>(ws + lay.work);
+    p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
+    p.ws_o = reinterpret_cast<float*>(ws + lay.o);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.group = num_q_heads / num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_context_len = max_context_len;
+    p.partition = plan.partition;
+    p.max_splits = plan.max_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.prefix_lens = prefix_lens;
+    p.split_base = 1;
+
+    PrefillParams pp;
+    pp.out = nullptr;
+    pp.q = q;
+    pp.cu_q_lens = group_offsets;
+    pp.q_start_pos = nullptr;
+    pp.seq_of_chunk = nullptr;
+    pp.k_cache = k_cache;
+    pp.v_cache = v_cache;
+    pp.block_tables = block_tables;
+    pp.context_lens = context_lens;
+    pp.error_count = error_count;
+    pp.num_chunks = num_groups;
+    pp.total_q = num_seqs;
+    pp.max_q_len = max_group_size;
+    pp.num_seqs = num_seqs;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.head_dim = head_dim;
+    pp.group = p.group;
+    pp.num_blocks = num_blocks;
+    pp.block_size = block_size;
+    pp.max_blocks_per_seq = max_blocks_per_seq;
+    pp.scale_log2 = p.scale_log2;
+    pp.prefix_lens = prefix_lens;
+    pp.part_o = p.ws_o;
+    pp.part_ml = p.ws_ml;
+    pp.part_splits = plan.max_splits;
+    if (!decode_tc_supported(p, dtype) || !prefill_tc_supported(pp, dtype)) return PA_ERR_UNSUPPORTED;
+
+    // prefix pass (each group's shared prefix once, on the tensor cores), tail pass, merge
+    if (num_groups > 0 && max_group_size > 0 && (rc = launch_prefill_tc(pp, st)) != PA_OK) return rc;
+    return run_decode(p, dtype, num_sms, st);
+}
+
 }  // extern "C"

@@ -80,6 +80,11 @@ struct DecodeParams {
     int* work;          // work[0]: next item, work[1]: finished CTAs (persistent kernel)
     float2* ws_ml;
     float* ws_o;
+    // Cascade tail pass: sequence s attends only tokens [prefix_lens[s], L); the
+    // shared prefix's partial sits in workspace slot 0 and the partitions'
+    // partials from slot split_base = 1 on.  nullptr / 0 for plain decode.
+    const int32_t* prefix_lens = nullptr;
+    int split_base = 0;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;
@@ -101,6 +106,17 @@ struct PrefillParams {
     int num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq;
     float scale_log2;
+    // Cascade prefix pass (pa_decode_cascade) when prefix_lens is set: chunk c
+    // is the group of decode sequences [cu_q_lens[c], cu_q_lens[c+1]), whose
+    // queries are those rows of q; every member attends keys [0, P) with
+    // P = prefix_lens[first member], read through the first member's table,
+    // and its partial (o, m, l) goes to slot 0 of part_o / part_ml (laid out
+    // like the decode workspace, part_splits slots per (sequence, kv head))
+    // instead of out.
+    const int32_t* prefix_lens = nullptr;
+    float* part_o = nullptr;
+    float2* part_ml = nullptr;
+    int part_splits = 0;
 };
 
 // Kernel launchers (defined in the .cu files).

@@ -75,7 +75,8 @@ int launch(const PrefillParams& p, cudaStream_t stream) {
 }  // namespace
 
 int launch_prefill_fma(const PrefillParams& p, int dtype, cudaStream_t stream) {
-    if (p.group > kFmaMaxGroup || p.num_chunks > 65535 || p.num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (p.group > kFmaMaxGroup || p.num_chunks > 65535 || p.num_kv_heads > 65535 || p.prefix_lens != nullptr)
+        return PA_ERR_UNSUPPORTED;
     if (dtype == PA_F32) return p.head_dim == 64 ? launch<float, 64>(p, stream) : launch<float, 128>(p, stream);
     return p.head_dim == 64 ? launch<__nv_bfloat16, 64>(p, stream) : launch<__nv_bfloat16, 128>(p, stream);
 }

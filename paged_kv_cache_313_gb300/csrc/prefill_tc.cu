@@ -47,8 +47,9 @@ constexpr int kHalf = 128 * 128; // bytes of one 64-column half of a 128-row til
 constexpr int kTileBytes = 2 * kHalf;
 constexpr int kThreads = 352;  // K producer, MMA issuer, 8 softmax warps, V producer
 constexpr int kVWarp = 10;
-constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O | row exchange (6 columns) | unused
-constexpr uint32_t kTmemXchg = 384;        // [tile parity][half] partial maxima, then [half] partial sums
+constexpr uint32_t kTmemCols = 512;        // S0 | S1 | O_a | O_b
+constexpr uint32_t kTmemOa = 256;          // keys 0-63 of every tile, softmax state of the row's first half
+constexpr uint32_t kTmemOb = 384;          // keys 64-127, the second half's state
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
 
@@ -97,12 +98,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos_per_tile = kTileQ / G;
 
     // ---- chunk descriptor (every thread, identical)
+    const bool prefix_mode = p.prefix_lens != nullptr;
     const int r0 = p.cu_q_lens[c];
     const int n = p.cu_q_lens[c + 1] - r0;
-    const int s = p.seq_of_chunk[c];
-    const int start = p.q_start_pos[c];
-    const bool chunk_ok = n >= 0 && r0 >= 0 && r0 + n <= p.total_q && n <= p.max_q_len && s >= 0 &&
-                          s < p.num_seqs && start >= 0;
+    const int s = prefix_mode ? r0 : p.seq_of_chunk[c];
+    int start = prefix_mode ? 0 : p.q_start_pos[c];
+    bool chunk_ok = n >= 0 && r0 >= 0 && r0 + n <= p.total_q && n <= p.max_q_len && s >= 0 && s < p.num_seqs;
+    if (chunk_ok && prefix_mode && n > 0) start = p.prefix_lens[s];  // the group's shared prefix length
+    chunk_ok = chunk_ok && start >= 0;
     if (!chunk_ok) {
         if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) count_error(p.error_count);
         return;
@@ -113,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i0 = tile * pos_per_tile;
     const int nq = min(pos_per_tile, n - i0);
     const int cap = min(p.context_lens[s], p.max_blocks_per_seq * B);
-    int last_key = start + i0 + nq - 1;  // the tile's last query position
+    // the tile's last query position; a cascade prefix pass reads keys [0, start) for every row
+    int last_key = prefix_mode ? start - 1 : start + i0 + nq - 1;
     if (last_key >= cap) {
         if (threadIdx.x == 0) count_error(p.error_count);
         last_key = cap - 1;
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
             const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
             const uint32_t v_base = smem_u32(smem + kV), p_base = smem_u32(smem + kP);
-            const uint32_t t_o = tmem + 256;
+            const uint32_t t_oa = tmem + kTmemOa, t_ob = tmem + kTmemOb;
             // descriptors of k-step 0; a k-step adds its byte offset >> 4 to the start-address field
             const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
@@ -273,7 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
                         const uint64_t poff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                        umma_bf16(t_o, dp + poff, dv + (uint64_t)((kk * 2048) >> 4), idesc_o, jj > 0 || kk > 0);
+                        // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
+                        umma_bf16(kk < 4 ? t_oa : t_ob, dp + poff, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                  jj > 0 || (kk & 3) > 0);
                     }
                     umma_commit(bars.o_done(pb));
                     umma_commit(bars.v_empty(vs));
@@ -284,19 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ============================================================ softmax / epilogue
-        // Eight warps: warps 2-5 take columns 0-63 of every row, warps 6-9 columns
-        // 64-127.  The two threads of a row exchange their partial maxima (and, at
-        // the end, their partial sums) through spare TMEM columns.  Every thread runs
-        // every iteration and every named barrier, even after a wait timed out, so
-        // the barrier can never be left one-sided.
+        // Eight warps: warps 2-5 take keys 0-63 of every tile (every row), warps 6-9
+        // keys 64-127.  Each half of a row runs its own online softmax (own max and
+        // sum) and its keys accumulate into their own O (O_a, O_b), so the two
+        // threads of a row never wait for each other inside the key loop; their
+        // states are combined once, in the epilogue.  Every thread runs every
+        // iteration and the named barrier, even after a wait timed out, so the
+        // barrier can never be left one-sided.
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;   // which 64 columns of the row
         const int r = quarter * 32 + lane;  // the query row this thread works on
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int col0 = half * 64;
+        const uint32_t t_own = tmem + lane_off + (half ? kTmemOb : kTmemOa);  // this half's O, row r
         const int pos = i0 + r / G;  // chunk-relative position
         const bool row_ok = pos - i0 < nq;
-        const int my_last = min(start + pos, last_key);  // last key this row may see
+        const int my_last = prefix_mode ? last_key : min(start + pos, last_key);  // last key this row may see
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         uint8_t* p_tile = smem + kP;
@@ -340,14 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mpart = fmaxf(mpart, sv[k]);
                 }
             }
-            // the row's two halves exchange partial maxima through a spare TMEM column pair
-            tmem_st1(tmem + lane_off + kTmemXchg + (j & 1) * 2 + half, mpart);
-            tmem_wait_st();
-            tc_fence_before();
-            softmax_bar();
-            tc_fence_after();
-            const float mt = fmaxf(mpart, tmem_ld1(tmem + lane_off + kTmemXchg + (j & 1) * 2 + (half ^ 1)));
-            tmem_wait_ld();
+            const float mt = mpart;
             if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
                 if (m_run != -INFINITY) {
                     const float alpha = fast_exp2(m_run - mt);
@@ -356,14 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // every PV issued so far (the last is PV_{j-1}) must be done before O changes
                         if (ok && !mbar_wait(bars.o_done((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
                         tc_fence_after();
-#pragma unroll
-                        for (int q2 = 0; q2 < 2; ++q2) {
-                            float t[32];
-                            tmem_ld32(tmem + lane_off + 256 + col0 + q2 * 32, t);
+#pragma unroll 1
+                        for (int q2 = 0; q2 < 8; ++q2) {  // all 128 columns of this half's O row
+                            float t[16];
+                            tmem_ld16(t_own + q2 * 16, t);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) t[i] *= alpha;
-                            tmem_st32(tmem + lane_off + 256 + col0 + q2 * 32, t);
+                            for (int i = 0; i < 16; ++i) t[i] *= alpha;
+                            tmem_st16(t_own + q2 * 16, t);
                         }
                         tmem_wait_st();
                     }
@@ -422,35 +424,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && nt > 0 && !mbar_wait(bars.o_done((nt - 1) & 1), ((nt - 1) >> 1) & 1)) ok = false;
         tc_fence_after();
         if (!ok && lane == 0) count_error(p.error_count);
-        tmem_st1(tmem + lane_off + kTmemXchg + 4 + half, l_run);
+        // combine the halves: M = max(m_a, m_b), O = (f_a O_a + f_b O_b) / (f_a l_a + f_b l_b),
+        // f_x = 2^(m_x - M); the states cross through TMEM columns 0-3 of S0 (free now)
+        tmem_st1(tmem + lane_off + half, m_run);
+        tmem_st1(tmem + lane_off + 2 + half, l_run);
         tmem_wait_st();
         tc_fence_before();
         softmax_bar();
         tc_fence_after();
-        const float l_row = l_run + tmem_ld1(tmem + lane_off + kTmemXchg + 4 + (half ^ 1));
+        const float m_oth = tmem_ld1(tmem + lane_off + (half ^ 1));
+        const float l_oth = tmem_ld1(tmem + lane_off + 2 + (half ^ 1));
         tmem_wait_ld();
+        const float m_a = half ? m_oth : m_run, m_b = half ? m_run : m_oth;
+        const float l_a = half ? l_oth : l_run, l_b = half ? l_run : l_oth;
+        const float m_row = fmaxf(m_a, m_b);
+        const float f_a = m_a == -INFINITY ? 0.f : fast_exp2(m_a - m_row);
+        const float f_b = m_b == -INFINITY ? 0.f : fast_exp2(m_b - m_row);
+        const float l_row = f_a * l_a + f_b * l_b;
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                             ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD + col0;
+        const float wa = f_a * inv, wb = f_b * inv;  // weights of O_a and O_b in this row's output
+        // member sequence r0 + pos, head r % G of a cascade prefix pass: its partial (o, m, l) goes to
+        // workspace slot 0; a member whose own prefix length differs from the group's gets an empty one
+        const int sm = r0 + pos;
+        const bool same = prefix_mode && row_ok && p.prefix_lens[sm] == start;
+        if (prefix_mode && row_ok && !same && half == 0 && r % G == 0) count_error(p.error_count);
+        const size_t slot = ((size_t)sm * p.num_kv_heads + kvh) * p.part_splits * G + (r % G);
+        if (prefix_mode && row_ok && half == 0)
+            p.part_ml[slot] = same ? make_float2(m_row, l_row) : make_float2(-INFINITY, 0.f);
+        __nv_bfloat16* out = prefix_mode ? nullptr
+                                         : static_cast<__nv_bfloat16*>(p.out) +
+                                               ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD +
+                                               col0;
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            float t[32];
+        for (int q4 = 0; q4 < 4; ++q4) {  // my 64 output columns, 16 at a time
+            float t[16];
             if (nt > 0) {
-                tmem_ld32(tmem + lane_off + 256 + col0 + q2 * 32, t);
+                float u[16];
+                tmem_ld16(tmem + lane_off + kTmemOa + col0 + q4 * 16, t);
+                tmem_ld16(tmem + lane_off + kTmemOb + col0 + q4 * 16, u);
                 tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) t[i] = t[i] * wa + u[i] * wb;
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) t[i] = 0.f;
+                for (int i = 0; i < 16; ++i) t[i] = 0.f;
             }
-            if (row_ok) {
+            if (!row_ok) continue;
+            if (prefix_mode) {
+                float4* po = reinterpret_cast<float4*>(p.part_o + slot * kD + col0 + q4 * 16);
+                const float f = same ? 1.f : 0.f;
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
+                for (int i = 0; i < 16; i += 4)
+                    po[i / 4] = make_float4(t[i] * f, t[i + 1] * f, t[i + 2] * f, t[i + 3] * f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; i += 8) {
                     uint4 pk;
-                    pk.x = pack_bf16x2(t[i] * inv, t[i + 1] * inv);
-                    pk.y = pack_bf16x2(t[i + 2] * inv, t[i + 3] * inv);
-                    pk.z = pack_bf16x2(t[i + 4] * inv, t[i + 5] * inv);
-                    pk.w = pack_bf16x2(t[i + 6] * inv, t[i + 7] * inv);
-                    *reinterpret_cast<uint4*>(out + q2 * 32 + i) = pk;
+                    pk.x = pack_bf16x2(t[i], t[i + 1]);
+                    pk.y = pack_bf16x2(t[i + 2], t[i + 3]);
+                    pk.z = pack_bf16x2(t[i + 4], t[i + 5]);
+                    pk.w = pack_bf16x2(t[i + 6], t[i + 7]);
+                    *reinterpret_cast<uint4*>(out + q4 * 16 + i) = pk;
                 }
             }
         }

@@ -19,8 +19,9 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_noalloc",
-           "pa_prefill_workspace_size", "pa_prefill_chunk", "pa_copy_blocks")
+           "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_cascade_workspace_size",
+           "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size", "pa_prefill_chunk",
+           "pa_copy_blocks")
 
 
 class PaError(RuntimeError):
@@ -43,6 +44,9 @@ _SIGNATURES = {
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
+    "pa_decode_cascade_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
+    "pa_decode_cascade": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _p, _i, _i, _p, _f, _p, _sz,
+                           _p, _p], _i),
     "pa_decode_noalloc": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p], _i),
     "pa_prefill_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_prefill_chunk": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _f, _p,
@@ -171,6 +175,39 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return out
+
+
+def new_cascade_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                          device=None) -> torch.Tensor:
+    """A zeroed workspace of the size pa_decode_cascade needs."""
+    n = int(lib().pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                                   max_context_len))
+    if n == 0:
+        raise PaError("pa_decode_cascade_workspace_size", PA_ERR_UNSUPPORTED, "unsupported sizes or device")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode_cascade(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, group_offsets,
+                      max_group_size: int, prefix_lens, scale: float, workspace, out=None, error_count=None,
+                      stream=None) -> torch.Tensor:
+    """pa_decode where each group of sequences [group_offsets[g], group_offsets[g+1]) shares its first
+    prefix_lens[s] context tokens: the shared prefix is read once per group (bf16, head_dim 128)."""
+    N, Hq, D = q.shape
+    P, B, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_cache differ")
+    if out is None:
+        out = torch.empty_like(q)
+    G = group_offsets.numel() - 1
+    _check("pa_decode_cascade", lib().pa_decode_cascade(
+        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len),
+        _dev(group_offsets, "group_offsets", torch.int32), G, int(max_group_size),
+        _dev(prefix_lens, "prefix_lens", torch.int32), float(scale), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev(error_count, "error_count", torch.int32),
+        _stream(stream)))
     return out
 
 

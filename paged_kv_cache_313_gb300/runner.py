@@ -15,7 +15,7 @@ from .workloads import Workload
 
 # Per-step inputs, in the order they sit in the packed input buffer, and outputs.
 STEP_INPUTS = ("q_decode", "k_new", "v_new", "block_tables", "context_lens", "seq_idx", "pos", "q_prefill",
-               "cu_q_lens", "q_start_pos", "seq_of_chunk")
+               "cu_q_lens", "q_start_pos", "seq_of_chunk", "group_offsets", "prefix_lens")
 STEP_OUTPUTS = ("out_decode", "out_prefill")
 _ALIGN = 256
 
@@ -42,7 +42,8 @@ def _packed_views(buf, like):
 
 
 class DeviceStep:
-    def __init__(self, w: Workload, device: str | torch.device = "cuda", with_error_count: bool = True):
+    def __init__(self, w: Workload, device: str | torch.device = "cuda", with_error_count: bool = True,
+                 cascade: bool = True):
         dev = torch.device(device)
         self.w = w
         self.device = dev
@@ -66,6 +67,13 @@ class DeviceStep:
         nd = w.num_decode
         self.workspace = (pa.new_decode_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                                   self.max_context_len, device=dev) if nd else None)
+        # cascade decode when decode sequences share prefixes (and the shapes allow it)
+        self.use_cascade = bool(cascade and nd and int(w.prefix_lens.max()) > 0 and w.dtype == torch.bfloat16
+                                and w.head_dim == 128 and w.num_q_heads // w.num_kv_heads in (1, 2, 4, 8)
+                                and w.block_size in (8, 16, 32, 64))
+        self.cascade_workspace = (pa.new_cascade_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                           w.block_size, self.max_context_len, device=dev)
+                                  if self.use_cascade else None)
         n = pa.pa_prefill_workspace_size(w.num_chunks, w.max_q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size) if w.num_chunks else 0
         self.prefill_workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=dev) if n else None
@@ -85,6 +93,11 @@ class DeviceStep:
         if not w.num_decode:
             return self.out_decode
         nd = w.num_decode
+        if self.use_cascade:
+            return pa.pa_decode_cascade(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
+                                        self.context_lens[:nd], self.max_context_len, self.group_offsets,
+                                        w.max_group_size, self.prefix_lens, w.scale, self.cascade_workspace,
+                                        out=self.out_decode, error_count=self.error_count, stream=stream)
         return pa.pa_decode(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
                             self.context_lens[:nd], self.max_context_len, w.scale, self.workspace,
                             out=self.out_decode, error_count=self.error_count, stream=stream)

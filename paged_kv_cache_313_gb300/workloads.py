@@ -25,6 +25,7 @@ import numpy as np
 import torch
 
 from .allocator import BlockAllocator, CowCopy
+from .cascade import cascade_groups
 
 WORKLOADS = ("tiny_fp32", "decode_bf16", "longctx_bf16", "shared_prefix_bf16", "mixed_bf16")
 
@@ -57,6 +58,10 @@ class Workload:
     meta: dict = field(default_factory=dict)
     allocator: BlockAllocator | None = None  # the allocator state that produced the tables
     seq_ids: list = field(default_factory=list)  # allocator ids of the table's rows
+    # decode sequences grouped by shared leading blocks (cascade.cascade_groups)
+    group_offsets: torch.Tensor | None = None  # int32 [G+1]
+    prefix_lens: torch.Tensor | None = None  # int32 [num_decode]
+    max_group_size: int = 0
 
     @property
     def num_seqs(self) -> int:
@@ -118,6 +123,7 @@ def _finish(name, dtype, Hq, Hkv, D, B, alloc: BlockAllocator, rng, decode_seqs,
     v_new = _normal(rng, (T, Hkv, D), dtype)
     q_decode = _normal(rng, (nd, Hq, D), dtype)
     q_prefill = _normal(rng, (cu[-1], Hq, D), dtype)
+    goff, pre, gmax = cascade_groups(bt[:nd].numpy(), ctx[:nd].numpy(), B)
     return Workload(
         name=name, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B, num_blocks=P,
         scale=scale if scale is not None else 1.0 / math.sqrt(D),
@@ -127,7 +133,8 @@ def _finish(name, dtype, Hq, Hkv, D, B, alloc: BlockAllocator, rng, decode_seqs,
         cu_q_lens=torch.tensor(cu, dtype=torch.int32),
         q_start_pos=torch.tensor(list(chunk_off), dtype=torch.int32),
         seq_of_chunk=torch.tensor([nd + i for i in range(len(chunk_off))], dtype=torch.int32),
-        q_prefill=q_prefill, cow_copies=list(cow), meta=dict(meta or {}), allocator=alloc, seq_ids=seqs)
+        q_prefill=q_prefill, cow_copies=list(cow), meta=dict(meta or {}), allocator=alloc, seq_ids=seqs,
+        group_offsets=torch.from_numpy(goff), prefix_lens=torch.from_numpy(pre), max_group_size=gmax)
 
 
 def _pool_size(needed_blocks: int, spare: float = 0.10) -> int:

@@ -277,3 +277,31 @@ def test_decode_plan_matches_workspace_and_launches():
     assert need >= 64 * 8 * splits * 4 * 128 * 4
     part1, splits1 = pa.pa_decode_plan(512, 32, 8, 128, 16, 300)
     assert splits1 == 1 and part1 >= 300
+
+
+@pytest.mark.parametrize("prefix_len,B", [(100, 16), (2048, 16), (160, 32)])
+def test_cascade_decode_matches_oracle_and_plain_decode(prefix_len, B):
+    """Cascade decode (each group's shared prefix read once, on the tensor
+    cores, merged with every member's private tail) against the oracle and
+    against plain paged decode of the same batch.  A 100-token prefix leaves
+    96 tokens in shared full blocks (not a multiple of 64: the tail pass masks
+    tokens 64..95 of its first stage) and the copied partial block in the tails."""
+    w = W.shared_prefix_bf16(3, num_prompts=3, branches=5, prefix_len=prefix_len, max_tail=70, B=B,
+                             name="cascade_case")
+    assert int(w.prefix_lens.max()) > 0
+    exp = expected_step(w)
+    cas = DeviceStep(w)
+    assert cas.use_cascade
+    cas.slot_mapping()
+    cas.write_kv()
+    got = cas.decode().clone()
+    plain = DeviceStep(w, cascade=False)
+    plain.run()
+    torch.cuda.synchronize()
+    assert cas.errors() == 0 and plain.errors() == 0
+    assert _maxabs(got, exp.out_decode) <= TOL[w.dtype]
+    assert (got.float() - plain.out_decode.float()).abs().max().item() <= TOL[w.dtype]
+    # repeat: bitwise identical
+    again = cas.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(again, got)
