@@ -17,7 +17,10 @@ time over eager launches, against the measured HBM copy bandwidth).  ``e2e`` re-
 memory: the step's packed inputs copied in from pinned memory (one copy), the
 step (graph replay unless ``--no-graph``), the packed outputs copied back (one
 copy), all inside the events.
-L2 is flushed (a 512 MiB write) before every timed step.  Under torchrun each
+L2 is flushed before every timed step: a 512 MiB write, then (default
+``--l2-flush write-read``) a 512 MiB read of another buffer, so that the
+write's dirty lines are written back before the timed step rather than
+inside it.  Under torchrun each
 rank runs an independent shard with its own seed (weak scaling, no collective
 on the data path).
 """
@@ -54,6 +57,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", choices=["write", "write-read"], default="write-read",
+                    help="between timed steps: write 512 MiB, and (write-read) then read another 512 MiB so "
+                         "that no dirty flush lines are written back inside a timed step")
     ap.add_argument("--no-cascade", dest="cascade", action="store_false",
                     help="plain paged decode even where decode sequences share prefixes")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
@@ -275,7 +281,7 @@ def run_reference(args):
     return 0
 
 
-def workload_config(w):
+def workload_config(w, l2_flush: str = "write"):
     ctx = [int(x) for x in w.context_lens[: w.num_decode]]
     cfg = {"workload": w.name, "decode_seqs": w.num_decode, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
            "head_dim": w.head_dim, "block_size": w.block_size, "num_blocks": w.num_blocks,
@@ -283,6 +289,9 @@ def workload_config(w):
            "prefill_chunks": w.num_chunks, "prefill_queries": int(w.cu_q_lens[-1]) if w.num_chunks else 0,
            "new_tokens": int(w.seq_idx.numel()), "seed": w.meta.get("seed", 0),
            "l2": "flushed before every timed step (512 MiB write)"}
+    if l2_flush == "write-read":
+        cfg["l2"] = ("flushed before every timed step: 512 MiB write, then a 512 MiB read of another buffer "
+                     "(dirty flush lines written back outside the timed events)")
     shared = int((w.prefix_lens > 0).sum()) if w.num_decode else 0
     if shared:
         cfg["shared_prefix_seqs"] = shared
@@ -310,6 +319,15 @@ def run_native(args):
     step = DeviceStep(w, dev, cascade=args.cascade)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    other = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.l2_flush == "write-read" else None
+
+    def flush_l2(v):
+        """Evict the step's data from L2 (outside the timed events): a 512 MiB write, then (write-read)
+        a 512 MiB read of another buffer, so that the flush's dirty lines are written back here and
+        not inside the next timed step."""
+        flush.fill_(v)
+        if other is not None:
+            torch.sum(other, dtype=torch.int32)
     decode_launches = 0
     if step.use_cascade:  # prefix pass, tail pass, merge
         decode_launches = 3
@@ -325,13 +343,13 @@ def run_native(args):
         torch.cuda.synchronize(dev)
 
     for _ in range(max(3, args.warmup)):
-        flush.fill_(1)
+        flush_l2(1)
         step.run()
     barrier()
     if args.graph:
         step.capture()
         for _ in range(3):
-            flush.fill_(1)
+            flush_l2(1)
             step.replay()
         barrier()
 
@@ -345,7 +363,7 @@ def run_native(args):
     barrier()
     t0 = time.time()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush_l2(i & 0xFF)
         ev[i][0].record(stream)
         if args.graph:
             step.replay()
@@ -361,7 +379,7 @@ def run_native(args):
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K1)]
     for i in range(K1):
         e = kev[i]
-        flush.fill_(i & 0xFF)
+        flush_l2(i & 0xFF)
         e[0].record(stream)
         step.slot_mapping()
         step.write_kv()
@@ -384,7 +402,7 @@ def run_native(args):
     e2e_ms = []
     K2 = max(1, min(K, 50))
     for i in range(K2):
-        flush.fill_(i & 0xFF)
+        flush_l2(i & 0xFF)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         step.run_from_host(host_in, host_out, graph=args.graph)
@@ -407,7 +425,7 @@ def run_native(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.l2_flush),
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
