@@ -14,24 +14,26 @@
 // (one box per physical block and 64-column half, 128-byte swizzled).
 //
 // Warp roles (352 threads):
-//   warp 0    TMA producer of the Q tile (once) and of K tiles into a 2-deep
+//   warp 0    TMA producer of the Q tile (once) and of K tiles into a 3-deep
 //             ring (released after their QK^T MMA); it also publishes each
 //             key tile's validity mask to the softmax warps.
-//   warp 10   TMA producer of V tiles into a 2-deep ring (released after their
+//   warp 10   TMA producer of V tiles into a 3-deep ring (released after their
 //             PV MMA); separate from warp 0 so K never queues behind V.
 //   warp 1    TMEM owner and MMA issuer (one thread):
 //               S_j = Q K_j^T      M=128 N=128 K=128   -> TMEM S[j%2]
-//               O  += P_j V_j      M=128 N=128 K=128   -> TMEM O
+//               O  += P_j V_j      M=128 N=128 K=128   A = P_j from TMEM
 //             S is double-buffered, so QK^T of tile j+1 runs on the tensor
-//             cores while the softmax warps work on tile j.
-//   warps 2-9 softmax, two threads per query row (TMEM lane = row, 64
-//             columns each, maxima exchanged through spare TMEM columns): read S,
-//             mask (causal and context), online softmax in base-2 units with
-//             a lazy rescale (O in TMEM is rescaled only when the row max
-//             grows by more than 2^8), write P as bf16 into one of two swizzled
-//             shared tiles for the PV MMA (so tile j+1 needs PV_j only when O
-//             must be rescaled), zero V rows past the last valid key, and
-//             finally normalise O and store the output rows.
+//             cores while the softmax warps work on tile j.  P_j is written
+//             over S_j in tensor memory and read from there as the A operand
+//             of the PV MMA, so shared memory holds only Q, K and V.
+//   warps 2-9 softmax, two threads per query row (TMEM lane = row), one for
+//             keys 0-63 and one for keys 64-127 of every tile, each with its
+//             own running max and sum and its own O accumulator (O_a, O_b),
+//             combined once at the end: read S, mask (causal and context),
+//             online softmax in base-2 units with a lazy rescale (a half's O is
+//             rescaled only when its max grows by more than 2^8), write P as
+//             bf16 into tensor memory, zero V rows past the last valid key,
+//             and finally normalise O and store the output rows.
 // All waits are bounded (an error is counted and the kernel still finishes);
 // TMEM is always freed.
 #include "pa_internal.cuh"
@@ -53,23 +55,22 @@ constexpr uint32_t kTmemOb = 384;          // keys 64-127, the second half's sta
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
 
-// shared memory layout (offsets from a 1024-aligned base)
+// shared memory layout (offsets from a 1024-aligned base).  P lives in tensor
+// memory (over the S buffer it was computed from), so shared memory holds Q
+// and 3-deep K and V rings.
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kMaskSlots = 8;  // the producer runs at most 5 key tiles ahead of the softmax's mask reads
 constexpr int kQ = 0;
-constexpr int kK = kQ + kTileBytes;      // 2 stages
-constexpr int kVStages = 2;
-constexpr int kV = kK + 2 * kTileBytes;  // 2 K stages
-constexpr int kP = kV + kVStages * kTileBytes;  // 2 P buffers
-constexpr int kBars = kP + 2 * kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full[2], o_done[2],
-// m_full[4]
-constexpr int kNumBars = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 4;
-constexpr int kMask = kBars + kNumBars * 8;  // uint32 [4][4]: key-validity mask of tile j in slot j%4
-constexpr int kTmemSlot = kMask + 4 * 4 * 4;
+constexpr int kK = kQ + kTileBytes;
+constexpr int kV = kK + kKStages * kTileBytes;
+constexpr int kBars = kV + kVStages * kTileBytes;
+// barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2], o_done[2], m_full[8]
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + kMaskSlots;
+constexpr int kMask = kBars + kNumBars * 8;  // uint32 [8][4]: key-validity mask of tile j in slot j%8
+constexpr int kTmemSlot = kMask + kMaskSlots * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
-
-__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
-    return row * 128u + ((chunk ^ (row & 7u)) << 4);
-}
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // the eight softmax warps (256 threads) only
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
@@ -78,14 +79,16 @@ struct Bars {
     uint64_t* base;
     __device__ uint64_t* q_full() const { return base; }
     __device__ uint64_t* k_full(int i) const { return base + 1 + i; }
-    __device__ uint64_t* k_empty(int i) const { return base + 3 + i; }
-    __device__ uint64_t* v_full(int i) const { return base + 5 + i; }
-    __device__ uint64_t* v_empty(int i) const { return base + 7 + i; }
-    __device__ uint64_t* s_full(int i) const { return base + 9 + i; }
-    __device__ uint64_t* s_empty(int i) const { return base + 11 + i; }
-    __device__ uint64_t* p_full(int i) const { return base + 13 + i; }  // P buffer i written
-    __device__ uint64_t* o_done(int i) const { return base + 15 + i; }  // the PV that read P buffer i is done
-    __device__ uint64_t* m_full(int i) const { return base + 17 + i; }  // mask slot i published
+    __device__ uint64_t* k_empty(int i) const { return base + 1 + kKStages + i; }
+    __device__ uint64_t* v_full(int i) const { return base + 1 + 2 * kKStages + i; }
+    __device__ uint64_t* v_empty(int i) const { return base + 1 + 2 * kKStages + kVStages + i; }
+    __device__ uint64_t* s_full(int i) const { return base + 1 + 2 * kKStages + 2 * kVStages + i; }
+    // P of tile j written into S buffer j%2
+    __device__ uint64_t* p_full(int i) const { return base + 3 + 2 * kKStages + 2 * kVStages + i; }
+    // the PV that read P buffer i is done
+    __device__ uint64_t* o_done(int i) const { return base + 5 + 2 * kKStages + 2 * kVStages + i; }
+    // mask slot i published
+    __device__ uint64_t* m_full(int i) const { return base + 7 + 2 * kKStages + 2 * kVStages + i; }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -134,21 +137,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bars.q_full(), 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(bars.k_full(i), 1);
             mbar_init(bars.k_empty(i), 1);
-            mbar_init(bars.s_full(i), 1);
-            mbar_init(bars.s_empty(i), 8);
         }
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(bars.v_full(i), 1);
             mbar_init(bars.v_empty(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.s_full(i), 1);
             mbar_init(bars.p_full(i), 8);
             mbar_init(bars.o_done(i), 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(bars.m_full(i), 1);
+        for (int i = 0; i < kMaskSlots; ++i) mbar_init(bars.m_full(i), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -208,14 +210,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
             const bool my_load = lane < bpt && b0 + lane < nblk && my_pb >= 0;
             if (!v_side) {
-                // K tile j (its slot is free once S_{j-2} completed, which also means the softmax
-                // warps have read mask j-4: they read a mask before releasing that tile's S)
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait(bars.k_empty(st), ((j - 2) >> 1) & 1)) ok = false;
+                // K tile j (its slot is free once S_{j-3} completed; S_{j-3} was issued after PV_{j-5}, so
+                // the softmax warps have finished tile j-5 and read every mask up to j-5: the mask ring
+                // of 8 slots is never overwritten unread)
+                const int st = j % kKStages;
+                if (j >= kKStages && !mbar_wait(bars.k_empty(st), ((j / kKStages) - 1) & 1)) ok = false;
                 if (!ok) break;
                 if (lane == 0) {
-                    for (int w = 0; w < 4; ++w) vmask[(j & 3) * 4 + w] = vm[w];
-                    mbar_arrive(bars.m_full(j & 3));
+                    for (int w = 0; w < 4; ++w) vmask[(j % kMaskSlots) * 4 + w] = vm[w];
+                    mbar_arrive(bars.m_full(j % kMaskSlots));
                     mbar_arrive_expect_tx(bars.k_full(st), bytes);
                 }
                 __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
@@ -244,42 +247,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
             const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
-            const uint32_t v_base = smem_u32(smem + kV), p_base = smem_u32(smem + kP);
+            const uint32_t v_base = smem_u32(smem + kV);
             const uint32_t t_oa = tmem + kTmemOa, t_ob = tmem + kTmemOb;
             // descriptors of k-step 0; a k-step adds its byte offset >> 4 to the start-address field
             const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
             const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
-            const uint64_t dp0 = umma_desc_sw128(p_base, 16, 1024);
             const uint64_t dv0 = umma_desc_sw128(v_base, kHalf, 1024);
             if (nt > 0 && !mbar_wait(bars.q_full(), 0)) ok = false;
             for (int j = 0; j <= nt && ok; ++j) {
                 if (j < nt) {  // S_j = Q K_j^T into S[j%2]
-                    const int st = j & 1;
-                    if (!mbar_wait(bars.k_full(st), (j >> 1) & 1)) { ok = false; break; }
-                    if (j >= 2 && !mbar_wait(bars.s_empty(st), ((j - 2) >> 1) & 1)) { ok = false; break; }
+                    // S[j%2] last held P_{j-2}, read by PV_{j-2}, which was issued before this MMA (the
+                    // tensor core runs one thread's MMAs in order)
+                    const int st = j % kKStages, sb = j & 1;
+                    if (!mbar_wait(bars.k_full(st), (j / kKStages) & 1)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                        umma_bf16(tmem + st * 128, dq0 + off, dk + off, idesc_s, kk > 0);
+                        umma_bf16(tmem + sb * 128, dq0 + off, dk + off, idesc_s, kk > 0);
                     }
-                    umma_commit(bars.s_full(st));
+                    umma_commit(bars.s_full(sb));
                     umma_commit(bars.k_empty(st));
                 }
-                if (j >= 1) {  // O += P_{j-1} V_{j-1}
+                if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from tensor memory
                     const int jj = j - 1, vs = jj % kVStages, pb = jj & 1;
                     if (!mbar_wait(bars.p_full(pb), (jj >> 1) & 1)) { ok = false; break; }
                     if (!mbar_wait(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t dp = dp0 + (uint64_t)((pb * kTileBytes) >> 4);
                     const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
-                        const uint64_t poff = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                        // keys 16kk..16kk+15: P columns 8kk.. (keys 0-63) or 64 + 8(kk-4).. (keys 64-127);
                         // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
-                        umma_bf16(kk < 4 ? t_oa : t_ob, dp + poff, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                  jj > 0 || (kk & 3) > 0);
+                        const uint32_t pa = tmem + pb * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                        umma_bf16_ta(kk < 4 ? t_oa : t_ob, pa, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                     jj > 0 || (kk & 3) > 0);
                     }
                     umma_commit(bars.o_done(pb));
                     umma_commit(bars.v_empty(vs));
@@ -308,15 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int my_last = prefix_mode ? last_key : min(start + pos, last_key);  // last key this row may see
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
-        uint8_t* p_tile = smem + kP;
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
             // validity of the tile's 128 keys (inside the context, in a block with a valid table
             // entry), published by the producer
-            if (ok && !mbar_wait(bars.m_full(j & 3), (j >> 2) & 1)) ok = false;
+            if (ok && !mbar_wait(bars.m_full(j % kMaskSlots), (j / kMaskSlots) & 1)) ok = false;
             uint32_t vm[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) vm[w] = vmask[(j & 3) * 4 + w];
+            for (int w = 0; w < 4; ++w) vm[w] = vmask[(j % kMaskSlots) * 4 + w];
             if (ok && !mbar_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
             tc_fence_after();
             float sv[64];
@@ -328,9 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i) sv[q2 * 32 + i] = t[i];
             }
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(bars.s_empty(st));
             const int kbase = j * kTileK + col0;
             const uint32_t w0 = vm[half * 2], w1 = vm[half * 2 + 1];
             // dense: every key of my 64 is valid and causally visible, and the scale is positive,
@@ -372,10 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 m_run = mt;
             }
-            // P = 2^(x - m) in bf16, my 64 columns of row r in P buffer j%2, which PV_{j-2} read
-            if (j >= 2 && ok && !mbar_wait(bars.o_done(j & 1), ((j - 2) >> 1) & 1)) ok = false;
-            tc_fence_after();
-            uint8_t* p_buf = p_tile + (j & 1) * kTileBytes;
+            // P = 2^(x - m) in bf16, my 64 keys of row r packed in pairs into 32 columns of S buffer j%2
+            // (its first 32 columns for keys 0-63, columns 64-95 for keys 64-127: each thread
+            // overwrites only S values it has already read)
             float lsum = 0.f;
             const float neg_m = -m_run;
             if (dense) {
@@ -386,20 +384,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 64; ++k)
                     sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
             }
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                float e[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    e[i] = sv[cc * 8 + i];
-                    lsum += e[i];
+                for (int i = 0; i < 32; ++i) {
+                    lsum += sv[2 * i] + sv[2 * i + 1];
+                    pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
                 }
-                uint4 pk;
-                pk.x = pack_bf16x2(e[0], e[1]);
-                pk.y = pack_bf16x2(e[2], e[3]);
-                pk.z = pack_bf16x2(e[4], e[5]);
-                pk.w = pack_bf16x2(e[6], e[7]);
-                *reinterpret_cast<uint4*>(p_buf + half * kHalf + swz(r, cc)) = pk;
+                tmem_st32u(tmem + lane_off + st * 128 + col0, pk);
+                tmem_wait_st();
             }
             l_run += lsum;
             // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
