@@ -335,7 +335,7 @@ def run_native(args):
         _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                       step.max_context_len)
         decode_launches = 1 + (1 if splits > 1 else 0)
-    launches_per_step = 2 + decode_launches + (1 if w.num_chunks else 0)
+    launches_per_step = 1 + decode_launches + (1 if w.num_chunks else 0)  # fused slot mapping + KV write first
 
     def barrier():
         if world > 1:
@@ -381,8 +381,7 @@ def run_native(args):
         e = kev[i]
         flush_l2(i & 0xFF)
         e[0].record(stream)
-        step.slot_mapping()
-        step.write_kv()
+        step.write_kv_paged()
         e[1].record(stream)
         step.decode()
         e[2].record(stream)
@@ -438,7 +437,7 @@ def run_native(args):
                      "logical_bytes_per_launch": logical_bytes,
                      "effective_gbs": logical_bytes / (mean_dec * 1e-3) / 1e9,
                      "traffic": recorded_traffic("pa_decode", w.name)},
-        "stage_ms": {"slot_mapping+write_kv": statistics.mean(write_ms), "decode": mean_dec,
+        "stage_ms": {"slot_mapping+write_kv (one launch)": statistics.mean(write_ms), "decode": mean_dec,
                      "prefill": statistics.mean(prefill_ms)},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2,

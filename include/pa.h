@@ -113,6 +113,21 @@ PA_API int pa_write_kv(const void* k_new, const void* v_new, int num_tokens, int
                 const int64_t* slot_mapping, int32_t* error_count, void* stream);
 
 /*
+ * pa_slot_mapping and pa_write_kv in one launch (the two steps the pages put
+ * between the scheduler and the attention kernel, fused): for every new
+ * token t the slot is resolved from (block_tables, seq_idx, pos) exactly as
+ * pa_slot_mapping does and the token's K and V rows are written there exactly
+ * as pa_write_kv does.  slot_mapping (int64 [num_tokens]) receives the slots
+ * when non-NULL.  Argument meaning, layouts, ownership and error counting are
+ * those of the two calls; the pools must not alias k_new / v_new.
+ */
+PA_API int pa_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads, int head_dim,
+                             int dtype, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                             const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                             const int32_t* seq_idx, const int32_t* pos, int64_t* slot_mapping,
+                             int32_t* error_count, void* stream);
+
+/*
  * Bytes of workspace pa_decode needs for these sizes (split-KV partial
  * results plus two work-queue counters).  Deterministic:
  * the same arguments on the same device always give the same size.

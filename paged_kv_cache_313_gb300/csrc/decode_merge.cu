@@ -44,6 +44,13 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
         const int first = pre > 0 ? 0 : p.split_base, ntot = p.split_base + nsplit;
         const int kvh = h / G, g = h - kvh * G;
         const size_t base = decode_unit(p, s, kvh) * p.max_splits * G + g;  // (slot 0, head g)
+        // the first kMergeUnroll partials' loads go out together with the (m, l) loads
+        const float4* o = reinterpret_cast<const float4*>(p.ws_o + base * D) + (lane < kLanes ? lane : 0);
+        const size_t stride4 = (size_t)G * D / 4;
+        float4 x[kMergeUnroll];
+#pragma unroll
+        for (int k = 0; k < kMergeUnroll; ++k)
+            if (first + k < ntot) x[k] = __ldcg(o + (size_t)(first + k) * stride4);
         // weights w_i = l_i 2^(m_i - m*) / sum: at most 128 slots, four per lane
         float2 v[4];
 #pragma unroll
@@ -66,19 +73,18 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[k] *= inv;
-        // out = sum_i w_i o_i
-        const float4* o = reinterpret_cast<const float4*>(p.ws_o + base * D) + (lane < kLanes ? lane : 0);
-        const size_t stride4 = (size_t)G * D / 4;
+        // out = sum_i w_i o_i, in slot order
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i0 = first; i0 < ntot; i0 += kMergeUnroll) {
-            float4 x[kMergeUnroll];
+            if (i0 != first) {
 #pragma unroll
-            for (int k = 0; k < kMergeUnroll; ++k)
-                if (i0 + k < ntot) x[k] = __ldcg(o + (size_t)(i0 + k) * stride4);
+                for (int k = 0; k < kMergeUnroll; ++k)
+                    if (i0 + k < ntot) x[k] = __ldcg(o + (size_t)(i0 + k) * stride4);
+            }
 #pragma unroll
             for (int k = 0; k < kMergeUnroll; ++k) {
                 const int i = i0 + k;
-                // weight of partition i lives in lane i % 32, slot i / 32
+                // weight of slot i lives in lane i % 32, register i / 32
                 const int slot = i >> 5;
                 const float wsrc = slot == 0 ? w[0] : slot == 1 ? w[1] : slot == 2 ? w[2] : w[3];
                 const float wi = __shfl_sync(0xffffffffu, wsrc, i & 31);

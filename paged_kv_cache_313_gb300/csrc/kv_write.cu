@@ -15,6 +15,25 @@
 namespace pa {
 namespace {
 
+// Slot of new token t, -1 when it is not written (pos < 0) or when its
+// sequence, logical block or table entry is out of range (counted).
+__device__ __forceinline__ long long slot_of(const int32_t* __restrict__ block_tables, int num_seqs,
+                                             int max_blocks_per_seq, const int32_t* __restrict__ seq_idx,
+                                             const int32_t* __restrict__ pos, int t, int block_size, int num_blocks,
+                                             int32_t* error_count) {
+    const int p = pos[t];
+    if (p < 0) return -1;
+    const int s = seq_idx[t];
+    const int logical_block = p / block_size;
+    const int offset = p - logical_block * block_size;
+    if (s >= 0 && s < num_seqs && logical_block < max_blocks_per_seq) {
+        const int physical = block_tables[(long long)s * max_blocks_per_seq + logical_block];
+        if (physical >= 0 && physical < num_blocks) return (long long)physical * block_size + offset;
+    }
+    count_error(error_count);
+    return -1;
+}
+
 __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int num_seqs, int max_blocks_per_seq,
                                     const int32_t* __restrict__ seq_idx, const int32_t* __restrict__ pos,
                                     int num_tokens, int block_size, int num_blocks, int64_t* __restrict__ slots,
@@ -23,21 +42,41 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, in
     pdl_wait();
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens) return;
-    int p = pos[t];
-    long long slot = -1;
-    if (p >= 0) {
-        int s = seq_idx[t];
-        int logical_block = p / block_size;
-        int offset = p - logical_block * block_size;
-        bool ok = s >= 0 && s < num_seqs && logical_block < max_blocks_per_seq;
-        if (ok) {
-            int physical = block_tables[(long long)s * max_blocks_per_seq + logical_block];
-            ok = physical >= 0 && physical < num_blocks;
-            if (ok) slot = (long long)physical * block_size + offset;
-        }
-        if (!ok) count_error(error_count);
+    slots[t] = slot_of(block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, t, block_size, num_blocks,
+                       error_count);
+}
+
+// Slot mapping and K/V scatter in one launch: one CTA per token; thread 0
+// resolves the slot (and records it when `slots` is given), then the CTA
+// copies the token's K and V rows with 16-byte accesses.
+__global__ void write_kv_paged_kernel(const int4* __restrict__ k_new, const int4* __restrict__ v_new, int row_vecs,
+                                      int4* __restrict__ k_cache, int4* __restrict__ v_cache,
+                                      const int32_t* __restrict__ block_tables, int num_seqs,
+                                      int max_blocks_per_seq, const int32_t* __restrict__ seq_idx,
+                                      const int32_t* __restrict__ pos, int block_size, int num_blocks,
+                                      int64_t* __restrict__ slots, int32_t* error_count) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ long long s_slot;
+    const int t = blockIdx.x;
+    if (threadIdx.x == 0) {
+        s_slot = slot_of(block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, t, block_size, num_blocks,
+                         error_count);
+        if (slots) slots[t] = s_slot;
     }
-    slots[t] = slot;
+    __syncthreads();
+    const long long slot = s_slot;
+    if (slot < 0) return;
+    const int4* ks = k_new + (long long)t * row_vecs;
+    const int4* vs = v_new + (long long)t * row_vecs;
+    int4* kd = k_cache + slot * row_vecs;
+    int4* vd = v_cache + slot * row_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        int4 k = __ldg(ks + i);
+        int4 v = __ldg(vs + i);
+        kd[i] = k;
+        vd[i] = v;
+    }
 }
 
 // One CTA per token: its K row and V row (row_bytes each, a multiple of 16)
@@ -109,6 +148,18 @@ int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int ro
                          static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs,
                          static_cast<int4*>(k_cache), static_cast<int4*>(v_cache), num_slots, slot_mapping,
                          error_count);
+}
+
+int launch_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
+                          void* v_cache, const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                          const int32_t* seq_idx, const int32_t* pos, int block_size, int num_blocks,
+                          int64_t* slot_mapping, int32_t* error_count, cudaStream_t stream) {
+    int row_vecs = row_bytes / 16;
+    int threads = row_vecs >= 256 ? 256 : ((row_vecs + 31) / 32) * 32;
+    return launch_kernel(write_kv_paged_kernel, dim3(num_tokens), dim3(threads), 0, stream,
+                         static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs,
+                         static_cast<int4*>(k_cache), static_cast<int4*>(v_cache), block_tables, num_seqs,
+                         max_blocks_per_seq, seq_idx, pos, block_size, num_blocks, slot_mapping, error_count);
 }
 
 int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,

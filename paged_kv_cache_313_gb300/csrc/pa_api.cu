@@ -179,6 +179,29 @@ int pa_write_kv(const void* k_new, const void* v_new, int num_tokens, int num_kv
                            static_cast<cudaStream_t>(stream));
 }
 
+int pa_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads, int head_dim,
+                      int dtype, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                      const int32_t* block_tables, int num_seqs, int max_blocks_per_seq, const int32_t* seq_idx,
+                      const int32_t* pos, int64_t* slot_mapping, int32_t* error_count, void* stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || num_blocks < 0 || block_size < 1 || num_seqs < 0 ||
+        max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !seq_idx || !pos ||
+        (num_seqs > 0 && max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_INVALID_ARG;
+    long long row_bytes = (long long)num_kv_heads * head_dim * elem_size(dtype);
+    if (row_bytes % 16 != 0 || row_bytes > (1 << 20)) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_UNSUPPORTED;
+    int rc = check_device(nullptr);
+    if (rc != PA_OK) return rc;
+    return launch_write_kv_paged(k_new, v_new, num_tokens, (int)row_bytes, k_cache, v_cache, block_tables, num_seqs,
+                                 max_blocks_per_seq, seq_idx, pos, block_size, num_blocks, slot_mapping, error_count,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int num_kv_heads, int head_dim,
                    int dtype, const int32_t* src_blocks, const int32_t* dst_blocks, const int32_t* num_valid,
                    int num_copies, int32_t* error_count, void* stream) {

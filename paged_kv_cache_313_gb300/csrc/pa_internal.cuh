@@ -127,6 +127,10 @@ int launch_slot_mapping(const int32_t* block_tables, int num_seqs, int max_block
 int launch_write_kv(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
                     void* v_cache, long long num_slots, const int64_t* slot_mapping, int32_t* error_count,
                     cudaStream_t stream);
+int launch_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, int row_bytes, void* k_cache,
+                          void* v_cache, const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                          const int32_t* seq_idx, const int32_t* pos, int block_size, int num_blocks,
+                          int64_t* slot_mapping, int32_t* error_count, cudaStream_t stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,
                        const int32_t* src, const int32_t* dst, const int32_t* num_valid, int num_copies,
                        int32_t* error_count, cudaStream_t stream);

@@ -19,9 +19,9 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_cascade_workspace_size",
-           "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size", "pa_prefill_chunk",
-           "pa_copy_blocks")
+           "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode",
+           "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
+           "pa_prefill_chunk", "pa_copy_blocks")
 
 
 class PaError(RuntimeError):
@@ -41,6 +41,7 @@ _SIGNATURES = {
     "pa_last_cuda_error": ([], _i),
     "pa_slot_mapping": ([_p, _i, _i, _p, _p, _i, _i, _i, _p, _p, _p], _i),
     "pa_write_kv": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _p, _p], _i),
+    "pa_write_kv_paged": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _i, _p, _p, _p, _p, _p], _i),
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
@@ -141,6 +142,24 @@ def pa_write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, error_count=None, 
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len) -> int:
     return int(lib().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                               max_context_len))
+
+
+def pa_write_kv_paged(k_new, v_new, k_cache, v_cache, block_tables, seq_idx, pos, slot_mapping=None,
+                      error_count=None, stream=None):
+    """Slot mapping and K/V scatter in one launch (bit-exact); slot_mapping, if given, receives the slots."""
+    T, H, D = k_new.shape
+    P, B = k_cache.shape[0], k_cache.shape[1]
+    S, W = block_tables.shape
+    for name, t in (("v_new", v_new), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != k_new.dtype:
+            raise TypeError(f"{name} dtype {t.dtype} differs from k_new {k_new.dtype}")
+    _check("pa_write_kv_paged", lib().pa_write_kv_paged(
+        _dev(k_new, "k_new"), _dev(v_new, "v_new"), T, H, D, _dtype_code(k_new), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), P, B, _dev(block_tables, "block_tables", torch.int32), S, W,
+        _dev(seq_idx, "seq_idx", torch.int32), _dev(pos, "pos", torch.int32),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(error_count, "error_count", torch.int32),
+        _stream(stream)))
+    return slot_mapping
 
 
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len):

@@ -88,6 +88,11 @@ class DeviceStep:
         pa.pa_write_kv(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
                        error_count=self.error_count, stream=stream)
 
+    def write_kv_paged(self, stream=None):
+        """Slot mapping and K/V write in one launch (the slots are still recorded)."""
+        pa.pa_write_kv_paged(self.k_new, self.v_new, self.k_cache, self.v_cache, self.block_tables, self.seq_idx,
+                             self.pos, slot_mapping=self.slots, error_count=self.error_count, stream=stream)
+
     def decode(self, stream=None):
         w = self.w
         if not w.num_decode:
@@ -112,9 +117,8 @@ class DeviceStep:
                                    error_count=self.error_count, stream=stream)
 
     def run(self, stream=None):
-        """The whole step: write this step's K/V, then attend."""
-        self.slot_mapping(stream)
-        self.write_kv(stream)
+        """The whole step: write this step's K/V (slot mapping and scatter in one launch), then attend."""
+        self.write_kv_paged(stream)
         self.decode(stream)
         self.prefill(stream)
         return self.out_decode, self.out_prefill

@@ -305,3 +305,36 @@ def test_cascade_decode_matches_oracle_and_plain_decode(prefix_len, B):
     again = cas.decode()
     torch.cuda.synchronize()
     assert torch.equal(again, got)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "mixed_bf16", "shared_prefix_bf16"])
+def test_fused_slot_mapping_and_write_matches_oracle(name):
+    """pa_write_kv_paged (slot mapping and scatter in one launch) writes exactly
+    the pools and slots the oracle's two steps give."""
+    w, exp = _case("small", name)
+    st = DeviceStep(w)
+    st.write_kv_paged()
+    torch.cuda.synchronize()
+    assert torch.equal(st.slots.cpu(), torch.from_numpy(exp.slots))
+    assert np.array_equal(storage_numpy(st.k_cache.cpu()), exp.k_cache)
+    assert np.array_equal(storage_numpy(st.v_cache.cpu()), exp.v_cache)
+    assert st.errors() == 0
+
+
+def test_fused_write_counts_invalid_entries_like_slot_mapping():
+    bt = torch.tensor([[3, -1], [0, 1]], dtype=torch.int32, device="cuda")
+    seq = torch.tensor([0, 0, 1, 1, 0, 2, -1, 1], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([5, -1, 9, 20, 17, 0, 0, 40], dtype=torch.int32, device="cuda")
+    kc = torch.zeros(4, 16, 2, 8, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kn = torch.arange(1, 8 * 16 + 1, dtype=torch.float32, device="cuda").view(8, 2, 8).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.empty(8, dtype=torch.int64, device="cuda")
+    pa.pa_write_kv_paged(kn, -kn, kc, vc, bt, seq, pos, slot_mapping=slots, error_count=err)
+    want, nerr = oracle.slot_mapping(bt.cpu().numpy(), seq.cpu().numpy(), pos.cpu().numpy(), 16, 4)
+    assert slots.cpu().tolist() == want.tolist() and int(err.item()) == nerr
+    flat_k, flat_v = kc.view(64, 16), vc.view(64, 16)
+    for t, sl in enumerate(want.tolist()):
+        if sl >= 0:
+            assert torch.equal(flat_k[sl], kn[t].view(16)) and torch.equal(flat_v[sl], -kn[t].view(16))
+    assert torch.count_nonzero(flat_k).item() == 16 * sum(1 for x in want.tolist() if x >= 0)
