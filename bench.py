@@ -396,6 +396,10 @@ def run_native(args):
     # pinned host memory (one copy), the step, the packed outputs copied back
     host_in = step.pinned_inputs()
     host_out = step.pinned_outputs()
+    step.step_from_host(host_in, host_out)
+    if args.graph:
+        step.capture_from_host(host_in, host_out)
+    barrier()
     h2d = host_in.numel() * host_in.element_size()
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []

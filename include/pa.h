@@ -266,6 +266,18 @@ PA_API int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, 
                      void* stream);
 
 /*
+ * Copy `bytes` from src to dst with a kernel on `stream`, where either buffer
+ * may be page-locked host memory (which the device addresses directly: on
+ * GB300 the CPU and GPU share a coherent link) or device memory.  For the
+ * per-step transfers of a serving loop (a packed input buffer in, the outputs
+ * out, a megabyte or less) this finishes sooner than the copy engine and can
+ * be captured into the same CUDA graph as the step.  Not part of the method:
+ * a deployment aid.  Both pointers and bytes must be multiples of 16;
+ * pageable (unregistered) host memory is rejected with PA_ERR_INVALID_ARG.
+ */
+PA_API int pa_stage_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * Copy-on-write block copy ([P1] 共享但不污染状态: a write into a shared
  * partial block first copies its valid entries into a private block).  For
  * each i < num_copies, token slots 0..num_valid[i]-1 of physical block

@@ -21,7 +21,7 @@ PA_F32, PA_BF16 = 0, 1
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
            "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
-           "pa_prefill_chunk", "pa_copy_blocks")
+           "pa_prefill_chunk", "pa_copy_blocks", "pa_stage_copy")
 
 
 class PaError(RuntimeError):
@@ -52,6 +52,7 @@ _SIGNATURES = {
     "pa_prefill_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_prefill_chunk": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _f, _p,
                           _sz, _p, _p], _i),
+    "pa_stage_copy": ([_p, _p, _sz, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _i, _p, _p], _i),
 }
 
@@ -286,3 +287,17 @@ def pa_copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, num_valid, error_co
         _dev(src_blocks, "src_blocks", torch.int32), _dev(dst_blocks, "dst_blocks", torch.int32),
         _dev(num_valid, "num_valid", torch.int32), src_blocks.numel(), _dev(error_count, "error_count", torch.int32),
         _stream(stream)))
+
+
+def pa_stage_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy src into dst (same number of bytes) with a kernel; either may be a pinned host tensor."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    n = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != n:
+        raise ValueError("dst and src sizes differ")
+    _check("pa_stage_copy", lib().pa_stage_copy(dst.data_ptr(), src.data_ptr(), n, _stream(stream)))
+    return dst

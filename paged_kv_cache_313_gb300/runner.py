@@ -163,16 +163,40 @@ class DeviceStep:
         _, views = _packed_views(host_out, [self.out_decode, self.out_prefill])
         return views
 
+    def step_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor, stream=None):
+        """One step from pinned host memory, eagerly: the packed inputs copied in
+        by a kernel reading the pinned buffer (pa_stage_copy), the step, the
+        packed outputs copied back the same way."""
+        pa.pa_stage_copy(self.inbuf, host_in, stream=stream)
+        self.run(stream)
+        pa.pa_stage_copy(host_out, self.outbuf, stream=stream)
+        return host_out
+
+    def capture_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor) -> "torch.cuda.CUDAGraph":
+        """Record copy-in, step and copy-out as one CUDA graph bound to these two
+        pinned buffers: a serving loop writes the next step's inputs into
+        host_in, replays, and reads host_out.  Call after one eager step."""
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.step_from_host(host_in, host_out)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_from_host(host_in, host_out)
+        self.host_graph = (g, host_in.data_ptr(), host_out.data_ptr())
+        return g
+
     def run_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor, graph: bool = True):
         """One step from pinned host memory: copy the packed inputs in, run the
-        step (the captured graph when there is one and `graph`), copy the
-        packed outputs back.  Asynchronous on the current stream."""
-        self.inbuf.copy_(host_in, non_blocking=True)
-        if graph and getattr(self, "graph", None) is not None:
-            self.graph.replay()
+        step, copy the packed outputs back — the captured graph of
+        capture_from_host when `graph` and it was captured for these buffers,
+        else eagerly.  Asynchronous on the current stream."""
+        hg = getattr(self, "host_graph", None)
+        if graph and hg is not None and hg[1] == host_in.data_ptr() and hg[2] == host_out.data_ptr():
+            hg[0].replay()
         else:
-            self.run()
-        host_out.copy_(self.outbuf, non_blocking=True)
+            self.step_from_host(host_in, host_out)
         return host_out
 
     def errors(self) -> int:

@@ -212,6 +212,33 @@ PREFILL_CASES = [
 ]
 
 
+DECODE_SHAPE_CASES = [
+    # (Hq, Hkv, D, B, decode context lengths, dtype): tensor-core decode at head_dim 64 and 128, every block
+    # size it takes and groups 1..8, partition boundaries (63/64/65, 512/513), and the CUDA-core path for
+    # group 16 and fp32
+    (8, 8, 64, 16, [1, 63, 64, 65, 700, 1300], torch.bfloat16),
+    (16, 8, 64, 8, [5, 512, 513, 2000], torch.bfloat16),
+    (64, 8, 128, 64, [1, 100, 4097], torch.bfloat16),
+    (32, 16, 128, 32, [3000, 17], torch.bfloat16),
+    (16, 2, 128, 8, [1025, 64], torch.bfloat16),
+    (128, 8, 128, 16, [300, 1], torch.bfloat16),
+    (8, 2, 128, 16, [9000, 33], torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_SHAPE_CASES)))
+def test_decode_shapes(case):
+    Hq, Hkv, D, B, lens, dt = DECODE_SHAPE_CASES[case]
+    w = W.prefill_batch(200 + case, Hq, Hkv, D, B, [], [], dtype=dt, decode_lens=lens)
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    err = _maxabs(st.out_decode, exp.out_decode)
+    assert err <= TOL[dt], f"decode max-abs error {err}"
+    assert st.errors() == 0
+
+
 @pytest.mark.parametrize("case", range(len(PREFILL_CASES)))
 def test_prefill_shapes(case):
     Hq, Hkv, B, lens, offs, dt = PREFILL_CASES[case]
@@ -248,8 +275,9 @@ def test_run_from_host_matches_device_step():
     w, _ = _case("small", "mixed_bf16")
     st = DeviceStep(w)
     want = [t.clone() for t in st.run()]
-    st.capture()
     host_in, host_out = st.pinned_inputs(), st.pinned_outputs()
+    st.step_from_host(host_in, host_out)
+    st.capture_from_host(host_in, host_out)
     for graph in (False, True):
         host_out.zero_()
         st.run_from_host(host_in, host_out, graph=graph)
@@ -338,3 +366,16 @@ def test_fused_write_counts_invalid_entries_like_slot_mapping():
         if sl >= 0:
             assert torch.equal(flat_k[sl], kn[t].view(16)) and torch.equal(flat_v[sl], -kn[t].view(16))
     assert torch.count_nonzero(flat_k).item() == 16 * sum(1 for x in want.tolist() if x >= 0)
+
+
+def test_stage_copy_moves_bytes_between_pinned_host_and_device():
+    g = torch.Generator().manual_seed(9)
+    host = torch.randint(0, 256, (1 << 20,), dtype=torch.uint8, generator=g).pin_memory()
+    dev = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    pa.pa_stage_copy(dev, host)
+    back = torch.zeros(1 << 20, dtype=torch.uint8).pin_memory()
+    pa.pa_stage_copy(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), host) and torch.equal(back, host)
+    with pytest.raises(ValueError):  # pageable host memory is refused before anything is launched
+        pa.pa_stage_copy(dev, torch.zeros(1 << 20, dtype=torch.uint8))
