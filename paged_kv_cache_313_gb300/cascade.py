@@ -15,12 +15,15 @@ from __future__ import annotations
 import numpy as np
 
 
-def cascade_groups(block_tables, context_lens, block_size: int, num_seqs: int | None = None):
+def cascade_groups(block_tables, context_lens, block_size: int, num_seqs: int | None = None,
+                   max_members: int | None = None):
     """Return (group_offsets int32 [G+1], prefix_lens int32 [N], max_group_size).
 
     block_tables: int [N, W] (rows beyond a sequence's blocks are ignored);
     context_lens: int [N].  Every sequence lands in exactly one group; a group
-    of one has prefix 0.
+    of one has prefix 0.  A run longer than max_members is cut into groups of
+    at most max_members (the decode kernel reads a group's queries as one tile
+    of at most 32 rows: max_members = 32 // (query heads per kv head)).
     """
     bt = np.asarray(block_tables)
     ctx = np.asarray(context_lens).astype(np.int64)
@@ -31,7 +34,8 @@ def cascade_groups(block_tables, context_lens, block_size: int, num_seqs: int | 
     while s < n:
         e = s + 1
         common = int(nblk[s])  # leading blocks the run shares with its first member
-        while common > 0 and e < n and nblk[e] > 0 and bt[e, 0] == bt[s, 0]:
+        while (common > 0 and e < n and nblk[e] > 0 and bt[e, 0] == bt[s, 0]
+               and (max_members is None or e - s < max_members)):
             k = min(common, int(nblk[e]))
             same = bt[s, :k] == bt[e, :k]
             common = k if same.all() else int(np.argmin(same))  # >= 1: the first blocks match

@@ -183,7 +183,10 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         }
         __syncthreads();
     }
-    const int total = s_total;
+    // items: the cascade groups' shared prefixes (one per group and kv head) first, then the
+    // (sequence, partition, kv head) items of the prefix sum
+    const int n_grouped = p.group_offsets ? p.num_groups * Hkv : 0;
+    const int total = s_total + n_grouped;
 
     if (warp == C::kConsumerWarps) {
         // ================================================================ producer
@@ -199,15 +202,36 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         while (item < total && ok) {
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(&work[0], 1);  // fetch the next item early
-            int s, split, kvh;
-            decode_item(cum, N, Hkv, item, s, split, kvh);
-            const int L = decode_context(p, s, false);
-            int pre;
-            const int j_first = decode_start(p, s, L, &pre);
-            const int nsplit = num_partitions(L - j_first, p.partition);
-            const bool direct = nsplit == 1 && pre == 0;
-            const int j0 = j_first + split * p.partition;
-            const int ntok = max(0, min(L, j0 + p.partition) - j0);
+            int s, split, kvh, nsplit, pre, j0, ntok;
+            const bool grouped = item < n_grouped;
+            if (grouped) {
+                // a cascade group's shared prefix for one kv head: tokens [0, P) of its first sequence,
+                // the group's G x members query rows at once (members * G <= 32)
+                const int g = item / Hkv;
+                kvh = item - g * Hkv;
+                s = p.group_offsets[g];
+                int members = p.group_offsets[g + 1] - s;
+                if (s < 0 || members < 1 || s + members > N || members * G > 32) {
+                    if (lane == 0) count_error(p.error_count);
+                    s = 0;
+                    members = 0;
+                }
+                const int L = members ? decode_context(p, s, false) : 0;
+                pre = 0;
+                if (members) decode_start(p, s, L, &pre);
+                nsplit = members;  // carried to the consumers in StageInfo::nsplit
+                split = pre;       // and the prefix length in StageInfo::split
+                j0 = 0;
+                ntok = pre;
+            } else {
+                decode_item(cum, N, Hkv, item - n_grouped, s, split, kvh);
+                const int L = decode_context(p, s, false);
+                const int j_first = decode_start(p, s, L, &pre);
+                nsplit = num_partitions(L - j_first, p.partition);
+                j0 = j_first + split * p.partition;
+                ntok = max(0, min(L, j0 + p.partition) - j0);
+            }
+            const bool direct = !grouped && nsplit == 1 && pre == 0;
             const int nst = max(1, (ntok + C::kStageTok - 1) / C::kStageTok);
             const int nblk = (ntok + B - 1) / B;
             const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq + j0 / B;
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     }
                 }
                 unsigned long long valid = 0ull;
-                uint32_t bytes = st == 0 ? (uint32_t)(G * D * 2) : 0u;
+                uint32_t bytes = st == 0 && !grouped ? (uint32_t)(G * D * 2) : 0u;
                 for (int b = 0; b < nb; ++b) {
                     const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
                     if (pb >= 0) {
@@ -246,7 +270,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                         bytes += 2u * C::kHalves * B * 128u;
                     }
                 }
-                const int skip = pre - (j0 + t0);  // tokens of a cascade prefix at the start of the stage
+                const int skip = grouped ? 0 : pre - (j0 + t0);  // a tail's first stage: mask the prefix tokens
                 if (skip > 0) valid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
                 if (lane == 0) {
                     StageInfo& inf = info[slot];
@@ -254,11 +278,11 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     inf.kvh = kvh;
                     inf.split = split;
                     inf.nsplit = nsplit;
-                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) | (direct ? 4 : 0);
+                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) | (direct ? 4 : 0) | (grouped ? 16 : 0);
                     inf.ntok = nt;
                     inf.valid = valid;
                     mbar_arrive_expect_tx(&full[slot], bytes);
-                    if (st == 0)
+                    if (st == 0 && !grouped)
                         bulk_load(smem + C::kQ + slot * C::kQBytes,
                                   static_cast<const __nv_bfloat16*>(p.q) +
                                       ((size_t)s * p.num_q_heads + (size_t)kvh * G) * D,
@@ -315,7 +339,19 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             }
             const StageInfo inf = info[slot];
             if (inf.s < 0) break;
-            if (inf.flags & 1) {  // first stage of an item: fresh state, load its queries
+            if ((inf.flags & 17) == 17) {  // first stage of a shared-prefix item: this warp's 8 rows from global
+                // row 8*warp + g4 is member (row / G), head (row % G) of the group's first sequence inf.s
+                const int rr = warp * 8 + g4, mem = rr / G, head = rr - mem * G;
+                const bool row_ok = mem < inf.nsplit;
+                const uint32_t* qg = reinterpret_cast<const uint32_t*>(
+                    static_cast<const __nv_bfloat16*>(p.q) +
+                    ((size_t)(inf.s + (row_ok ? mem : 0)) * p.num_q_heads + (size_t)inf.kvh * G + head) * D);
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    qb[kk][0] = row_ok ? __ldg(qg + kk * 8 + c4) : 0u;
+                    qb[kk][1] = row_ok ? __ldg(qg + kk * 8 + c4 + 4) : 0u;
+                }
+            } else if (inf.flags & 1) {  // first stage of an item: load its queries
                 const uint8_t* qs = smem + C::kQ + slot * C::kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < KT; ++kk) {
@@ -326,15 +362,17 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                         qb[kk][0] = qb[kk][1] = 0u;
                     }
                 }
+            }
+            if (inf.flags & 1) {  // fresh softmax state
 #pragma unroll
                 for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
             }
-            const uint32_t rows = (uint32_t)(inf.valid >> row0) & 0xFFFFu;  // validity of this warp's rows
-            if (row0 < inf.ntok) {
-                uint8_t* kt = smem + C::kRing + slot * C::kStageBytes;
-                uint8_t* vt = kt + C::kTileBytes;
+            uint8_t* kt = smem + C::kRing + slot * C::kStageBytes;
+            uint8_t* vt = kt + C::kTileBytes;
+            // 16 token rows r0c..r0c+15 of the stage against this warp's 8 query rows (validity `rows`)
+            auto chunk16 = [&](const int r0c, const uint32_t rows) {
                 if (rows != 0xFFFFu) {  // zero V rows without a valid token
                     const int r = lane >> 1;
                     if (!((rows >> r) & 1u)) {
@@ -343,7 +381,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<int4*>(vt + tr.row(row0 + r) + h * tr.half_stride +
+                                *reinterpret_cast<int4*>(vt + tr.row(r0c + r) + h * tr.half_stride +
                                                          ((lane & 1) * 4 + c) * 16) = z;
                     }
                     __syncwarp();
@@ -351,7 +389,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 // S^T = K Q^T (two independent accumulation chains)
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
                 {
-                    const uint32_t r = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const uint32_t kbase = smem_u32(kt);
 #pragma unroll
                     for (int kk = 0; kk < KT; ++kk) {
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));
                 const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));
                 {  // O^T += V^T P^T
-                    const uint32_t r = row0 + (lane & 7) + (lane >> 4) * 8;
+                    const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
                     const uint32_t vbase = smem_u32(vt);
 #pragma unroll
                     for (int mt = 0; mt < KT; ++mt) {
@@ -405,9 +443,54 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     }
                 }
                 if (rows != 0xFFFFu) fence_proxy_async_smem();  // zeroing before the slot's next TMA write
+            };
+            if (inf.flags & 16) {
+                // a shared-prefix item: this warp's 8 query rows against all 64 tokens of the stage (every warp
+                // zeroes the invalid V rows of a chunk before it reads them; the writes are identical)
+#pragma unroll 1
+                for (int r0c = 0; r0c < inf.ntok; r0c += 16) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
+            } else if (row0 < inf.ntok) {
+                chunk16(row0, (uint32_t)(inf.valid >> row0) & 0xFFFFu);
             }
             __syncwarp();
             if (!(inf.flags & 2)) {
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                continue;
+            }
+            if (inf.flags & 16) {
+                // ---------------------------------------- shared-prefix item epilogue
+                // This warp's 8 rows are its own: normalise them and store every member's prefix
+                // partial (o, m, l) in workspace slot 0.  A member whose own prefix length differs
+                // from the group's gets an empty partial and an error count.
+                float L0 = l0, L1 = l1;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+                    L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+                }
+#pragma unroll
+                for (int hsel = 0; hsel < 2; ++hsel) {
+                    const int rr = warp * 8 + 2 * c4 + hsel, mem = rr / G, head = rr - mem * G;
+                    if (mem >= inf.nsplit) continue;
+                    const int sm = inf.s + mem;
+                    int pre_m;
+                    decode_start(p, sm, decode_context(p, sm, false), &pre_m);
+                    const bool same = pre_m == inf.split;  // inf.split carries the group's prefix length
+                    const size_t slot0 = decode_unit(p, sm, inf.kvh) * p.max_splits * G + head;
+                    const float Ls = hsel ? L1 : L0;
+                    const float inv = (same && Ls > 0.f) ? 1.f / Ls : 0.f;
+                    float* wo = p.ws_o + slot0 * D;
+#pragma unroll
+                    for (int mt = 0; mt < KT; ++mt) {
+                        wo[mt * 16 + g4] = o[mt][hsel] * inv;
+                        wo[mt * 16 + g4 + 8] = o[mt][2 + hsel] * inv;
+                    }
+                    if (g4 == 0) {
+                        p.ws_ml[slot0] = same ? make_float2(hsel ? m1 : m0, Ls) : make_float2(-INFINITY, 0.f);
+                        if (!same) count_error(p.error_count);
+                    }
+                }
+                __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
                 continue;
             }

@@ -346,6 +346,13 @@ int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const i
 
 // ---- cascade decode: shared prefixes read once per group
 
+// 1: the decode kernel reads each group's prefix as one item of its queue
+// (groups of at most 32 query rows); 0: the tensor-core prefill kernel's
+// prefix mode reads them in a separate launch.
+#ifndef PA_CASCADE_PREFIX_IN_DECODE
+#define PA_CASCADE_PREFIX_IN_DECODE 1
+#endif
+
 // Plan of the cascade: the tail pass uses pa_decode's partitions, and slot 0 of
 // every (sequence, kv head) holds the prefix partial, so max_splits grows by one.
 static DecodePlan plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
@@ -450,6 +457,12 @@ int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_heads, i
     if (!decode_tc_supported(p, dtype) || !prefill_tc_supported(pp, dtype)) return PA_ERR_UNSUPPORTED;
 
     // prefix pass (each group's shared prefix once, on the tensor cores), tail pass, merge
+    if (PA_CASCADE_PREFIX_IN_DECODE && max_group_size * p.group <= 32) {
+        // the shared prefixes are items of the decode kernel's own queue (one per group and kv head)
+        p.group_offsets = group_offsets;
+        p.num_groups = num_groups;
+        return run_decode(p, dtype, num_sms, st);
+    }
     if (num_groups > 0 && max_group_size > 0 && (rc = launch_prefill_tc(pp, st)) != PA_OK) return rc;
     return run_decode(p, dtype, num_sms, st);
 }

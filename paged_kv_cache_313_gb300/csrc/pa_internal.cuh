@@ -85,6 +85,10 @@ struct DecodeParams {
     // partials from slot split_base = 1 on.  nullptr / 0 for plain decode.
     const int32_t* prefix_lens = nullptr;
     int split_base = 0;
+    // Cascade prefix items: group g = sequences [group_offsets[g], group_offsets[g+1]) shares
+    // prefix_lens[group_offsets[g]] leading tokens; the decode kernel reads them once per group.
+    const int32_t* group_offsets = nullptr;
+    int num_groups = 0;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;

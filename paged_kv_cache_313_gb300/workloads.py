@@ -123,7 +123,7 @@ def _finish(name, dtype, Hq, Hkv, D, B, alloc: BlockAllocator, rng, decode_seqs,
     v_new = _normal(rng, (T, Hkv, D), dtype)
     q_decode = _normal(rng, (nd, Hq, D), dtype)
     q_prefill = _normal(rng, (cu[-1], Hq, D), dtype)
-    goff, pre, gmax = cascade_groups(bt[:nd].numpy(), ctx[:nd].numpy(), B)
+    goff, pre, gmax = cascade_groups(bt[:nd].numpy(), ctx[:nd].numpy(), B, max_members=max(1, 32 // (Hq // Hkv)))
     return Workload(
         name=name, dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B, num_blocks=P,
         scale=scale if scale is not None else 1.0 / math.sqrt(D),

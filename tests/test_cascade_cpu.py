@@ -44,3 +44,11 @@ def test_unshared_batches_are_singletons():
     w = W.small("decode_bf16", 0)
     assert w.group_offsets.tolist() == list(range(w.num_decode + 1))
     assert int(w.prefix_lens.max()) == 0 and w.max_group_size == 1
+
+
+def test_runs_longer_than_the_tile_are_cut():
+    bt = np.array([[7, 8]] * 5 + [[1, 2]], np.int32)
+    ctx = np.array([30] * 5 + [30], np.int32)
+    off, pre, mx = cascade_groups(bt, ctx, 16, max_members=2)
+    assert off.tolist() == [0, 2, 4, 5, 6] and mx == 2
+    assert pre.tolist() == [30, 30, 30, 30, 0, 0]  # a group of one keeps no prefix
