@@ -329,8 +329,8 @@ def run_native(args):
         if other is not None:
             other.view(torch.int64).sum()  # a plain read of the 512 MiB (no widening copy)
     decode_launches = 0
-    if step.use_cascade:  # prefix pass, tail pass, merge
-        decode_launches = 3
+    if step.use_cascade:  # decode (prefix items + tails) and merge; a separate prefix pass for groups over 32 rows
+        decode_launches = 2 if w.max_group_size * (w.num_q_heads // w.num_kv_heads) <= 32 else 3
     elif w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
         _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                       step.max_context_len)
@@ -432,7 +432,7 @@ def run_native(args):
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
-                     "kernel": ("pa_decode_cascade (prefill_tc_kernel prefix pass + decode_tc_kernel tails + "
+                     "kernel": ("pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; "
                                 "decode_merge_kernel)" if step.use_cascade
                                 else "pa_decode (decode_tc_kernel + decode_merge_kernel)"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",

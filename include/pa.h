@@ -190,10 +190,13 @@ PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, in
  *     through the group's first member's block table, and a member whose
  *     prefix length differs from the first member's is counted in error_count.
  *   - max_group_size >= the largest group.
- * Three kernels run on `stream`: the prefix pass (the group's queries, G per
- * sequence, stacked as the rows of a tensor-core tile against the prefix's
- * keys), the tail pass (each sequence's tokens [prefix_len, L)), and the
- * log-sum-exp merge of the two.  workspace: pa_decode_cascade_workspace_size
+ * Two kernels run on `stream`: the decode kernel, whose queue holds one item
+ * per (group, kv head) for the shared prefix (the group's G x members query
+ * rows against the prefix's keys, at most 32 rows) followed by the
+ * (sequence, partition, kv head) items of every sequence's own tokens
+ * [prefix_len, L), and the log-sum-exp merge of the two.  A group wider than
+ * 32 query rows has its prefix read by a third, tensor-core prefill-style
+ * kernel first.  workspace: pa_decode_cascade_workspace_size
  * bytes, 256-byte aligned, zeroed once.  Supported: bf16, head_dim 128,
  * num_q_heads/num_kv_heads in {1, 2, 4, 8}, block_size 8..64; otherwise
  * PA_ERR_UNSUPPORTED (use pa_decode).

@@ -379,3 +379,23 @@ def test_stage_copy_moves_bytes_between_pinned_host_and_device():
     assert torch.equal(dev.cpu(), host) and torch.equal(back, host)
     with pytest.raises(ValueError):  # pageable host memory is refused before anything is launched
         pa.pa_stage_copy(dev, torch.zeros(1 << 20, dtype=torch.uint8))
+
+
+def test_cascade_groups_wider_than_a_tile_use_the_prefill_prefix_pass():
+    """A group of 12 sequences x 4 heads (48 query rows) is more than the
+    decode kernel's 32-row tile: pa_decode_cascade reads its prefix with the
+    tensor-core prefill kernel's prefix pass instead; same results."""
+    w = W.shared_prefix_bf16(7, num_prompts=2, branches=12, prefix_len=160, max_tail=50, B=16, name="wide_groups")
+    exp = expected_step(w)
+    st = DeviceStep(w, cascade=False)
+    st.write_kv_paged()
+    nd = w.num_decode
+    offs = torch.tensor([0, 12, 24], dtype=torch.int32, device="cuda")
+    pre = torch.full((nd,), 160, dtype=torch.int32, device="cuda")
+    ws = pa.new_cascade_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, st.max_context_len)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = pa.pa_decode_cascade(st.q_decode, st.k_cache, st.v_cache, st.block_tables[:nd], st.context_lens[:nd],
+                               st.max_context_len, offs, 12, pre, w.scale, ws, error_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _maxabs(got, exp.out_decode) <= TOL[w.dtype]
