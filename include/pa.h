@@ -269,6 +269,22 @@ PA_API int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, 
                      void* stream);
 
 /*
+ * Kernel-side block tables for a block manager whose blocks hold `ratio`
+ * kernel blocks ("PagedAttention学习笔记", 代码实现部分 › 块表与槽位映射, 混合块:
+ * map_to_kernel_blocks).  The manager's pool [P][ratio*B][Hkv][D] is the same
+ * memory as the kernels' pool [P*ratio][B][Hkv][D], so manager block m maps to
+ * kernel blocks m*ratio .. m*ratio+ratio-1 and every slot is unchanged:
+ *   kernel_tables[s][j] = mgr_tables[s][j / ratio] * ratio + j % ratio
+ * (-1 where the manager entry is -1 or j / ratio >= mgr_width).
+ *   mgr_tables     int32 [num_seqs][mgr_width], read
+ *   kernel_tables  int32 [num_seqs][kernel_width], written (kernel_width is
+ *                  normally mgr_width * ratio)
+ * Returns PA_ERR_INVALID_ARG for negative sizes or ratio < 1.
+ */
+PA_API int pa_map_to_kernel_blocks(const int32_t* mgr_tables, int num_seqs, int mgr_width, int ratio,
+                                   int32_t* kernel_tables, int kernel_width, void* stream);
+
+/*
  * Copy `bytes` from src to dst with a kernel on `stream`, where either buffer
  * may be page-locked host memory (which the device addresses directly: on
  * GB300 the CPU and GPU share a coherent link) or device memory.  For the

@@ -52,6 +52,8 @@ def _load():
             lib.oracle_num_blocks.argtypes = [i64, i64]
             lib.oracle_num_blocks.restype = i64
             lib.oracle_slot_mapping.argtypes = [i32p, i64, i64, i32p, i32p, i64, i64, i64, i64p]
+            lib.oracle_map_to_kernel_blocks.argtypes = [i32p, i64, i64, i64, i32p, i64]
+            lib.oracle_map_to_kernel_blocks.restype = None
             lib.oracle_slot_mapping.restype = ctypes.c_int
             lib.oracle_write_kv.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, i64, i64, i64p]
             lib.oracle_write_kv.restype = ctypes.c_int
@@ -96,6 +98,17 @@ def slot_mapping(block_tables, seq_idx, pos, block_size: int, num_blocks: int):
     rc = _load().oracle_slot_mapping(btp, bt.shape[0], bt.shape[1], sip, psp, si.shape[0], block_size,
                                      num_blocks, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
     return out, -rc
+
+
+def map_to_kernel_blocks(mgr_tables, ratio: int, kernel_width: int | None = None):
+    """Kernel-side block tables for manager blocks of ratio kernel blocks each."""
+    mt, mtp = _i32(mgr_tables)
+    S, W = mt.shape
+    kw = W * ratio if kernel_width is None else int(kernel_width)
+    out = np.empty((S, kw), dtype=np.int32)
+    _load().oracle_map_to_kernel_blocks(mtp, S, W, int(ratio), out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        kw)
+    return out
 
 
 def write_kv(k_new, v_new, k_cache, v_cache, slots) -> int:

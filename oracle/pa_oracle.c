@@ -78,6 +78,28 @@ int oracle_slot_mapping(const int32_t* block_tables, int64_t num_seqs, int64_t m
     return -errors;
 }
 
+/* [P2] 代码实现部分 › "块表与槽位映射：BlockTable" (混合块, map_to_kernel_blocks):
+ * when the block manager allocates blocks of ratio x kernel_block_size tokens,
+ * each manager block is the same memory as `ratio` consecutive kernel blocks,
+ * so manager block m becomes kernel blocks m*ratio, m*ratio+1, ...,
+ * m*ratio+ratio-1, in order; a -1 entry becomes ratio -1 entries.  Row s of
+ * the kernel table has kernel_width entries; positions past the manager
+ * table's ratio*mgr_width are -1. */
+void oracle_map_to_kernel_blocks(const int32_t* mgr_tables, int64_t num_seqs, int64_t mgr_width,
+                                 int64_t ratio, int32_t* kernel_tables, int64_t kernel_width) {
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        for (int64_t j = 0; j < kernel_width; ++j) {
+            int64_t m = j / ratio;
+            int32_t entry = -1;
+            if (m < mgr_width) {
+                int32_t mb = mgr_tables[s * mgr_width + m];
+                if (mb >= 0) entry = (int32_t)(mb * ratio + j % ratio);
+            }
+            kernel_tables[s * kernel_width + j] = entry;
+        }
+    }
+}
+
 /* [P3] "对 ModelRunner 的影响": the slot tells where the current token's K/V is
  * written.  A byte copy of each token's [num_kv_heads][head_dim] row into the
  * pool row at its slot; slot < 0 is skipped, slot beyond the pool is an error. */

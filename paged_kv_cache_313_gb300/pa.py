@@ -21,7 +21,7 @@ PA_F32, PA_BF16 = 0, 1
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
            "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
-           "pa_prefill_chunk", "pa_copy_blocks", "pa_stage_copy")
+           "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy")
 
 
 class PaError(RuntimeError):
@@ -53,6 +53,7 @@ _SIGNATURES = {
     "pa_prefill_chunk": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _f, _p,
                           _sz, _p, _p], _i),
     "pa_stage_copy": ([_p, _p, _sz, _p], _i),
+    "pa_map_to_kernel_blocks": ([_p, _i, _i, _i, _p, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _i, _p, _p], _i),
 }
 
@@ -301,3 +302,15 @@ def pa_stage_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Te
         raise ValueError("dst and src sizes differ")
     _check("pa_stage_copy", lib().pa_stage_copy(dst.data_ptr(), src.data_ptr(), n, _stream(stream)))
     return dst
+
+
+def pa_map_to_kernel_blocks(mgr_tables, ratio: int, kernel_tables=None, stream=None) -> torch.Tensor:
+    """Kernel block tables for manager blocks of `ratio` kernel blocks: entry j of row s is
+    mgr_tables[s, j // ratio] * ratio + j % ratio (-1 for -1)."""
+    S, W = mgr_tables.shape
+    if kernel_tables is None:
+        kernel_tables = torch.empty(S, W * ratio, dtype=torch.int32, device=mgr_tables.device)
+    _check("pa_map_to_kernel_blocks", lib().pa_map_to_kernel_blocks(
+        _dev(mgr_tables, "mgr_tables", torch.int32), S, W, int(ratio),
+        _dev(kernel_tables, "kernel_tables", torch.int32), kernel_tables.shape[1], _stream(stream)))
+    return kernel_tables

@@ -399,3 +399,65 @@ def test_cascade_groups_wider_than_a_tile_use_the_prefill_prefix_pass():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert _maxabs(got, exp.out_decode) <= TOL[w.dtype]
+
+
+def test_map_to_kernel_blocks_matches_oracle_and_decode_through_it():
+    """Manager blocks of 64 tokens (4 kernel blocks of 16): the device remap equals the oracle's, and
+    decode through the remapped table on the same pool gives the oracle's decode through the manager
+    table (the pool [P][64][Hkv][D] read as [4P][16][Hkv][D])."""
+    rng = np.random.default_rng(31)
+    ratio, Bk, Hq, Hkv, D = 4, 16, 32, 8, 128
+    Bm = ratio * Bk
+    lens = np.array([1, 64, 65, 700, 2000, 333], np.int32)
+    nb = -(-lens // Bm)
+    P = int(nb.sum()) + 3
+    perm = rng.permutation(P).astype(np.int32)
+    mgr = np.full((len(lens), int(nb.max())), -1, np.int32)
+    at = 0
+    for s, n in enumerate(nb):
+        mgr[s, :n] = perm[at:at + n]
+        at += n
+    kc = rng.standard_normal((P, Bm, Hkv, D), dtype=np.float32)
+    vc = rng.standard_normal((P, Bm, Hkv, D), dtype=np.float32)
+    q = rng.standard_normal((len(lens), Hq, D), dtype=np.float32)
+    want_tables = oracle.map_to_kernel_blocks(mgr, ratio)
+    got_tables = pa.pa_map_to_kernel_blocks(torch.from_numpy(mgr).cuda(), ratio)
+    assert np.array_equal(got_tables.cpu().numpy(), want_tables)
+    want = oracle.decode(q, kc, vc, mgr, lens, 1.0 / math.sqrt(D))  # manager view, block size 64
+    bf = lambda x: torch.from_numpy(x).to(torch.bfloat16).cuda()  # noqa: E731
+    kk = bf(kc).view(P * ratio, Bk, Hkv, D)
+    vv = bf(vc).view(P * ratio, Bk, Hkv, D)
+    want_bf = oracle.decode(bf(q).float().cpu().numpy(), bf(kc).float().cpu().numpy(),
+                            bf(vc).float().cpu().numpy(), mgr, lens, 1.0 / math.sqrt(D))
+    got = _decode_direct(bf(q), kk, vv, got_tables, torch.from_numpy(lens).cuda(), int(lens.max()),
+                         1.0 / math.sqrt(D))
+    assert _maxabs(got, want_bf) <= TOL[torch.bfloat16]
+    assert np.abs(want_bf - want).max() < 0.1  # bf16 inputs vs fp32 inputs: same attention
+
+
+def test_multi_layer_pools_share_one_slot_mapping():
+    """A 3-layer pool [layers][P][B][Hkv][D] ("KV cache 显存管理…": the cache is per layer, the block table
+    is not): one slot mapping per step, then per layer the write and the decode on that layer's slice,
+    each equal to the oracle's on that layer."""
+    w, _ = _case("small", "decode_bf16")
+    layers = 3
+    rng = np.random.default_rng(41)
+    P, B, Hkv, D = w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim
+    nd, T = w.num_decode, int(w.seq_idx.numel())
+    mk = lambda *shape: torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)  # noqa
+    kpool, vpool = mk(layers, P, B, Hkv, D), mk(layers, P, B, Hkv, D)
+    knew, vnew, q = mk(layers, T, Hkv, D), mk(layers, T, Hkv, D), mk(layers, nd, w.num_q_heads, D)
+    dk, dv = kpool.cuda(), vpool.cuda()
+    bt, ctx = w.block_tables.cuda(), w.context_lens.cuda()
+    slots = pa.pa_slot_mapping(bt, w.seq_idx.cuda(), w.pos.cuda(), B, P)
+    for layer in range(layers):
+        pa.pa_write_kv(knew[layer].cuda(), vnew[layer].cuda(), dk[layer], dv[layer], slots)
+        got = _decode_direct(q[layer].cuda(), dk[layer], dv[layer], bt[:nd], ctx[:nd], w.max_decode_context,
+                             w.scale)
+        kc, vc = storage_numpy(kpool[layer]).copy(), storage_numpy(vpool[layer]).copy()
+        sl, _ = oracle.slot_mapping(w.block_tables.numpy(), w.seq_idx.numpy(), w.pos.numpy(), B, P)
+        oracle.write_kv(storage_numpy(knew[layer]), storage_numpy(vnew[layer]), kc, vc, sl)
+        assert np.array_equal(storage_numpy(dk[layer].cpu()), kc)
+        want = oracle.decode(storage_numpy(q[layer]), kc, vc, w.block_tables.numpy()[:nd],
+                             w.context_lens.numpy()[:nd], w.scale)
+        assert _maxabs(got, want) <= TOL[torch.bfloat16]

@@ -313,3 +313,34 @@ def test_prefill_first_position_and_causal_limit():
     # a chunk that ends beyond the sequence's context is rejected
     with pytest.raises(ValueError):
         oracle.prefill(q, cu, qs, soc, kc, vc, bt, np.array([36, 21], np.int32), 0.35)
+
+
+# ---- manager-block -> kernel-block remap ("PagedAttention学习笔记", 块表与槽位映射, 混合块)
+
+def test_map_to_kernel_blocks_worked_example():
+    # the 40-token sequence of the worked example with 32-token manager blocks 7, 2 (and a padding entry):
+    # with 16-token kernel blocks, manager block 7 is kernel blocks 14, 15 and block 2 is 4, 5
+    got = oracle.map_to_kernel_blocks(np.array([[7, 2, -1]], np.int32), 2)
+    assert got.tolist() == [[14, 15, 4, 5, -1, -1]]
+
+
+def test_map_to_kernel_blocks_keeps_every_slot():
+    """Every position's slot through the manager table (block size ratio*B) equals its slot through the
+    kernel table (block size B): the remap changes the bookkeeping, never the address."""
+    rng = np.random.default_rng(21)
+    for ratio, Bk in ((2, 16), (4, 8), (3, 16), (1, 32)):
+        Bm = ratio * Bk
+        P = 9
+        L = rng.integers(1, 4 * Bm, size=5)
+        width = int(-(-L.max() // Bm))
+        mgr = np.full((5, width), -1, np.int32)
+        for s in range(5):
+            nb = -(-int(L[s]) // Bm)
+            mgr[s, :nb] = rng.permutation(P)[:nb]
+        kern = oracle.map_to_kernel_blocks(mgr, ratio)
+        seq = np.repeat(np.arange(5, dtype=np.int32), [int(x) for x in L])
+        pos = np.concatenate([np.arange(int(x), dtype=np.int32) for x in L])
+        s_mgr, e1 = oracle.slot_mapping(mgr, seq, pos, Bm, P)
+        s_ker, e2 = oracle.slot_mapping(kern, seq, pos, Bk, P * ratio)
+        assert e1 == e2 == 0
+        assert np.array_equal(s_mgr, s_ker)
