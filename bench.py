@@ -335,7 +335,8 @@ def run_native(args):
         _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                       step.max_context_len)
         decode_launches = 1 + (1 if splits > 1 else 0)
-    launches_per_step = 1 + decode_launches + (1 if w.num_chunks else 0)  # fused slot mapping + KV write first
+    write_launches = 0 if step.fused_decode_write and not w.num_chunks else 1  # slot mapping + KV write
+    launches_per_step = write_launches + decode_launches + (1 if w.num_chunks else 0)
 
     def barrier():
         if world > 1:
@@ -381,9 +382,9 @@ def run_native(args):
         e = kev[i]
         flush_l2(i & 0xFF)
         e[0].record(stream)
-        step.write_kv_paged()
+        step.write_stage()
         e[1].record(stream)
-        step.decode()
+        step.decode_stage()
         e[2].record(stream)
         step.prefill()
         e[3].record(stream)
@@ -420,6 +421,8 @@ def run_native(args):
 
     hbm, bf16_tf, bf16_tf_sus, peak_kind = peaks()
     alg_bytes = decode_algorithmic_bytes(w)  # each physical K/V slot once
+    if step.fused_decode_write:  # the decode tokens' new K/V rows: read from k_new/v_new, written to the pools
+        alg_bytes += 2 * w.num_decode * w.kv_bytes_per_token()
     logical_bytes = decode_algorithmic_bytes(w, unique=False)  # every sequence's whole context
     achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
     tokens = sharding.total_units(w.num_decode)
@@ -434,6 +437,8 @@ def run_native(args):
         "roofline": {"bound": "hbm",
                      "kernel": ("pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; "
                                 "decode_merge_kernel)" if step.use_cascade
+                                else "pa_decode_write (decode_tc_kernel with the decode tokens' KV write + "
+                                     "decode_merge_kernel)" if step.fused_decode_write
                                 else "pa_decode (decode_tc_kernel + decode_merge_kernel)"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
@@ -441,7 +446,7 @@ def run_native(args):
                      "logical_bytes_per_launch": logical_bytes,
                      "effective_gbs": logical_bytes / (mean_dec * 1e-3) / 1e9,
                      "traffic": recorded_traffic("pa_decode", w.name)},
-        "stage_ms": {"slot_mapping+write_kv (one launch)": statistics.mean(write_ms), "decode": mean_dec,
+        "stage_ms": {"kv_write (separate launch)": statistics.mean(write_ms), "decode": mean_dec,
                      "prefill": statistics.mean(prefill_ms)},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2,

@@ -211,6 +211,29 @@ PA_API int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_h
                              void* workspace, size_t workspace_bytes, int32_t* error_count, void* stream);
 
 /*
+ * pa_decode fused with the KV write of the step's decode tokens: sequence s's
+ * newest token (position L-1, L = context_lens[s]) has its K and V rows in
+ * k_new / v_new ([num_seqs][num_kv_heads][head_dim], read).  The decode
+ * kernel writes them into k_cache / v_cache at the slot the block table gives
+ * (block_tables[s][(L-1)/B]*B + (L-1)%B, exactly pa_slot_mapping +
+ * pa_write_kv for that token) and attends with them, so the step needs no
+ * separate write launch for its decode tokens ("KV cache 显存管理…",
+ * 对 ModelRunner 的影响: the write slots and the attention inputs arrive
+ * together).  new_slots (int64 [num_seqs], may be NULL) receives the slots.
+ * Everything else is pa_decode's.  A sequence whose newest token falls in a
+ * block with an invalid table entry is counted in error_count and nothing is
+ * written for it.  Supported: bf16 and the shapes of the tensor-core decode
+ * kernel (head_dim 64 or 128, num_q_heads/num_kv_heads <= 8, block_size 8,
+ * 16, 32 or 64); otherwise PA_ERR_UNSUPPORTED (use pa_write_kv + pa_decode).
+ */
+PA_API int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int dtype, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                           const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                           int max_context_len, float scale, const void* k_new, const void* v_new,
+                           int64_t* new_slots, void* workspace, size_t workspace_bytes, int32_t* error_count,
+                           void* stream);
+
+/*
  * pa_decode for callers that cannot allocate device memory.  The pages have
  * no counterpart: this is a deployment aid, not part of the method.
  *

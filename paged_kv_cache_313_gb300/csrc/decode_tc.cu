@@ -63,6 +63,8 @@ struct StageInfo {
     int flags;  // bit 0: first stage of its item, bit 1: last stage, bit 2: the item writes the output
     int ntok;   // tokens of this stage (0..64)
     unsigned long long valid;  // bit r: token row r holds a valid token
+    int new_row;         // pa_decode_write: row of the sequence's newest token in this stage, or -1
+    long long new_slot;  // and its pool slot
 };
 
 template <int D>
@@ -79,7 +81,10 @@ struct TcCfg {
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kRing = 0;
     static constexpr int kQ = kRing + kStages * kStageBytes;
-    static constexpr int kCum = kQ + kStages * kQBytes;  // int [kMaxSeqs + 1]
+    // pa_decode_write: the newest token's K and V rows of the item, staged next to each stage
+    static constexpr int kNew = kQ + kStages * kQBytes;
+    static constexpr int kNewBytes = 2 * D * 2;
+    static constexpr int kCum = kNew + kStages * kNewBytes;  // int [kMaxSeqs + 1]
     static constexpr int kInfo = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
     static constexpr int kEnd = kBars + 2 * kStages * 8;
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
         while (item < total && ok) {
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(&work[0], 1);  // fetch the next item early
-            int s, split, kvh, nsplit, pre, j0, ntok;
+            int s, split, kvh, nsplit, pre, j0, ntok, L_item = 0;
             const bool grouped = item < n_grouped;
             if (grouped) {
                 // a cascade group's shared prefix for one kv head: tokens [0, P) of its first sequence,
@@ -226,6 +231,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             } else {
                 decode_item(cum, N, Hkv, item - n_grouped, s, split, kvh);
                 const int L = decode_context(p, s, false);
+                L_item = L;
                 const int j_first = decode_start(p, s, L, &pre);
                 nsplit = num_partitions(L - j_first, p.partition);
                 j0 = j_first + split * p.partition;
@@ -272,6 +278,20 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 }
                 const int skip = grouped ? 0 : pre - (j0 + t0);  // a tail's first stage: mask the prefix tokens
                 if (skip > 0) valid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
+                // pa_decode_write: the sequence's newest token (position L - 1) falls in this stage
+                int new_row = -1;
+                long long new_slot = -1;
+                if (p.k_new && !grouped) {
+                    const int jn = L_item - 1 - (j0 + t0);
+                    if (L_item > 0 && jn >= 0 && jn < nt) {
+                        const int pbn = __shfl_sync(0xffffffffu, pb_lane, (b0 + jn / B) & 31);
+                        if (pbn >= 0) {
+                            new_row = jn;
+                            new_slot = (long long)pbn * B + (L_item - 1) % B;
+                            bytes += (uint32_t)C::kNewBytes;
+                        }
+                    }
+                }
                 if (lane == 0) {
                     StageInfo& inf = info[slot];
                     inf.s = s;
@@ -281,7 +301,16 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) | (direct ? 4 : 0) | (grouped ? 16 : 0);
                     inf.ntok = nt;
                     inf.valid = valid;
+                    inf.new_row = new_row;
+                    inf.new_slot = new_slot;
                     mbar_arrive_expect_tx(&full[slot], bytes);
+                    if (new_row >= 0) {
+                        const size_t row = ((size_t)s * Hkv + kvh) * D;
+                        bulk_load(smem + C::kNew + slot * C::kNewBytes,
+                                  static_cast<const __nv_bfloat16*>(p.k_new) + row, (uint32_t)(D * 2), &full[slot]);
+                        bulk_load(smem + C::kNew + slot * C::kNewBytes + D * 2,
+                                  static_cast<const __nv_bfloat16*>(p.v_new) + row, (uint32_t)(D * 2), &full[slot]);
+                    }
                     if (st == 0 && !grouped)
                         bulk_load(smem + C::kQ + slot * C::kQBytes,
                                   static_cast<const __nv_bfloat16*>(p.q) +
@@ -450,6 +479,22 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
 #pragma unroll 1
                 for (int r0c = 0; r0c < inf.ntok; r0c += 16) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
             } else if (row0 < inf.ntok) {
+                if (inf.new_row >= row0 && inf.new_row < row0 + 16) {
+                    // pa_decode_write: the newest token's staged K and V rows go into this stage's tiles
+                    // (128-byte swizzled, before any ldmatrix of the row) and into the pool at its slot
+                    const uint8_t* stg = smem + C::kNew + slot * C::kNewBytes;
+                    constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+                    for (int c = lane; c < 2 * kChunks; c += 32) {
+                        const int isv = c >= kChunks, cc = isv ? c - kChunks : c;
+                        const int4 v = *reinterpret_cast<const int4*>(stg + isv * D * 2 + cc * 16);
+                        *reinterpret_cast<int4*>((isv ? vt : kt) + tr.at(inf.new_row, cc / 8, cc % 8)) = v;
+                        __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(isv ? p.v_write : p.k_write);
+                        reinterpret_cast<int4*>(pool + ((size_t)inf.new_slot * Hkv + inf.kvh) * D)[cc] = v;
+                    }
+                    if (p.new_slots && inf.kvh == 0 && lane == 0) p.new_slots[inf.s] = inf.new_slot;
+                    fence_proxy_async_smem();  // these writes precede the slot's next TMA write
+                    __syncwarp();
+                }
                 chunk16(row0, (uint32_t)(inf.valid >> row0) & 0xFFFFu);
             }
             __syncwarp();

@@ -249,48 +249,91 @@ int pa_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
     return PA_OK;
 }
 
+// Checks and parameters shared by pa_decode and pa_decode_write; *p is ready
+// for run_decode when PA_OK is returned.
+static int prepare_decode(DecodeParams* p, int* num_sms, void* out, const void* q, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int dtype, const void* k_cache, const void* v_cache,
+                          int num_blocks, int block_size, const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int max_context_len, float scale, void* workspace,
+                          size_t workspace_bytes, int32_t* error_count) {
+    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
+    if (rc != PA_OK) return rc;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_cache || !v_cache || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_INVALID_ARG;
+    if ((rc = check_device(num_sms)) != PA_OK) return rc;
+    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, *num_sms, SIZE_MAX);
+    DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    p->out = out;
+    p->q = q;
+    p->k_cache = k_cache;
+    p->v_cache = v_cache;
+    p->block_tables = block_tables;
+    p->context_lens = context_lens;
+    p->error_count = error_count;
+    p->work = reinterpret_cast<int*>(ws + lay.work);
+    p->ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
+    p->ws_o = reinterpret_cast<float*>(ws + lay.o);
+    p->num_seqs = num_seqs;
+    p->num_q_heads = num_q_heads;
+    p->num_kv_heads = num_kv_heads;
+    p->head_dim = head_dim;
+    p->group = num_q_heads / num_kv_heads;
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->max_blocks_per_seq = max_blocks_per_seq;
+    p->max_context_len = max_context_len;
+    p->partition = plan.partition;
+    p->max_splits = plan.max_splits;
+    p->scale_log2 = scale * 1.4426950408889634f;
+    return PA_OK;
+}
+
 int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int dtype,
               const void* k_cache, const void* v_cache, int num_blocks, int block_size,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
               int max_context_len, float scale, void* workspace, size_t workspace_bytes, int32_t* error_count,
               void* stream) {
-    if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
-    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
-    if (rc != PA_OK) return rc;
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
-        return PA_ERR_INVALID_ARG;
-    int num_sms = 0;
-    if ((rc = check_device(&num_sms)) != PA_OK) return rc;
-    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
-    DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
-    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return PA_ERR_WORKSPACE;
-    char* ws = static_cast<char*>(workspace);
+    if (num_seqs == 0 && num_blocks >= 0 && max_blocks_per_seq >= 0 && max_context_len >= 0 &&
+        decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size) == PA_OK &&
+        (dtype == PA_F32 || dtype == PA_BF16))
+        return PA_OK;
     DecodeParams p;
-    p.out = out;
-    p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.error_count = error_count;
-    p.work = reinterpret_cast<int*>(ws + lay.work);
-    p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml);
-    p.ws_o = reinterpret_cast<float*>(ws + lay.o);
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.head_dim = head_dim;
-    p.group = num_q_heads / num_kv_heads;
-    p.num_blocks = num_blocks;
-    p.block_size = block_size;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.max_context_len = max_context_len;
-    p.partition = plan.partition;
-    p.max_splits = plan.max_splits;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    int num_sms = 0;
+    int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, dtype, k_cache,
+                            v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, scale, workspace, workspace_bytes, error_count);
+    if (rc != PA_OK) return rc;
+    return run_decode(p, dtype, num_sms, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                    int dtype, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                    int max_context_len, float scale, const void* k_new, const void* v_new, int64_t* new_slots,
+                    void* workspace, size_t workspace_bytes, int32_t* error_count, void* stream) {
+    if (num_seqs == 0 && num_blocks >= 0 && max_blocks_per_seq >= 0 && max_context_len >= 0 &&
+        decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size) == PA_OK && dtype == PA_BF16)
+        return PA_OK;
+    if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_UNSUPPORTED;
+    DecodeParams p;
+    int num_sms = 0;
+    int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, dtype, k_cache,
+                            v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, scale, workspace, workspace_bytes, error_count);
+    if (rc != PA_OK) return rc;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_write = k_cache;
+    p.v_write = v_cache;
+    p.new_slots = new_slots;
+    if (!decode_tc_supported(p, dtype)) return PA_ERR_UNSUPPORTED;  // the fused write lives in the tensor-core kernel
     return run_decode(p, dtype, num_sms, static_cast<cudaStream_t>(stream));
 }
 

@@ -89,6 +89,14 @@ struct DecodeParams {
     // prefix_lens[group_offsets[g]] leading tokens; the decode kernel reads them once per group.
     const int32_t* group_offsets = nullptr;
     int num_groups = 0;
+    // pa_decode_write: the newest token of each sequence (position L - 1) has its K and V rows in
+    // k_new / v_new [num_seqs][num_kv_heads][head_dim]; the decode kernel writes them into the pools
+    // (k_write / v_write = k_cache / v_cache) and attends with them; new_slots[s] gets the slot.
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
+    void* k_write = nullptr;
+    void* v_write = nullptr;
+    int64_t* new_slots = nullptr;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;

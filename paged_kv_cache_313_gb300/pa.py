@@ -19,7 +19,7 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode",
+           "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_write",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
            "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy")
 
@@ -45,6 +45,8 @@ _SIGNATURES = {
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
+    "pa_decode_write": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p, _p, _p, _sz, _p,
+                         _p], _i),
     "pa_decode_cascade_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode_cascade": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _p, _i, _i, _p, _f, _p, _sz,
                            _p, _p], _i),
@@ -194,6 +196,26 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
         _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return out
+
+
+def pa_decode_write(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float, k_new,
+                    v_new, workspace, out=None, new_slots=None, error_count=None, stream=None) -> torch.Tensor:
+    """pa_decode that also writes each sequence's newest token (K/V rows k_new/v_new [N, Hkv, D]) into the
+    pools at its slot, in the same launch."""
+    N, Hq, D = q.shape
+    P, B, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(k_new.shape) != (N, Hkv, D) or tuple(v_new.shape) != (N, Hkv, D):
+        raise ValueError("shapes of q, k_cache, k_new, v_new disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode_write", lib().pa_decode_write(
+        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
+        _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype), _dev(new_slots, "new_slots", torch.int64),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
     return out

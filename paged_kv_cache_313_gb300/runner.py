@@ -43,7 +43,7 @@ def _packed_views(buf, like):
 
 class DeviceStep:
     def __init__(self, w: Workload, device: str | torch.device = "cuda", with_error_count: bool = True,
-                 cascade: bool = True):
+                 cascade: bool = True, fused_decode_write: bool = True):
         dev = torch.device(device)
         self.w = w
         self.device = dev
@@ -74,6 +74,14 @@ class DeviceStep:
         self.cascade_workspace = (pa.new_cascade_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                                            w.block_size, self.max_context_len, device=dev)
                                   if self.use_cascade else None)
+        # decode tokens written by the decode kernel itself (pa_decode_write) when the step's first nd new
+        # tokens are the decode sequences' newest ones and the shapes are the tensor-core decode kernel's
+        G = w.num_q_heads // w.num_kv_heads
+        newest = bool(nd) and torch.equal(w.seq_idx[:nd], torch.arange(nd, dtype=w.seq_idx.dtype)) and \
+            torch.equal(w.pos[:nd], w.context_lens[:nd].to(w.pos.dtype) - 1)
+        self.fused_decode_write = bool(fused_decode_write and newest and not self.use_cascade
+                                       and w.dtype == torch.bfloat16 and w.head_dim in (64, 128) and G <= 8
+                                       and w.block_size in (8, 16, 32, 64))
         n = pa.pa_prefill_workspace_size(w.num_chunks, w.max_q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size) if w.num_chunks else 0
         self.prefill_workspace = torch.zeros(max(n, 1), dtype=torch.uint8, device=dev) if n else None
@@ -116,10 +124,32 @@ class DeviceStep:
                                    w.scale, workspace=self.prefill_workspace, out=self.out_prefill,
                                    error_count=self.error_count, stream=stream)
 
+    def write_stage(self, stream=None):
+        """The step's KV writes that are not done by the decode kernel itself."""
+        if not self.fused_decode_write:
+            self.write_kv_paged(stream)
+            return
+        nd = self.w.num_decode
+        if self.k_new.shape[0] > nd:  # the prefill chunks' tokens
+            pa.pa_write_kv_paged(self.k_new[nd:], self.v_new[nd:], self.k_cache, self.v_cache, self.block_tables,
+                                 self.seq_idx[nd:], self.pos[nd:], slot_mapping=self.slots[nd:],
+                                 error_count=self.error_count, stream=stream)
+
+    def decode_stage(self, stream=None):
+        """Decode as the step runs it: fused with the decode tokens' KV write when possible."""
+        if not self.fused_decode_write:
+            return self.decode(stream)
+        w, nd = self.w, self.w.num_decode
+        return pa.pa_decode_write(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
+                                  self.context_lens[:nd], self.max_context_len, w.scale, self.k_new[:nd],
+                                  self.v_new[:nd], self.workspace, out=self.out_decode, new_slots=self.slots[:nd],
+                                  error_count=self.error_count, stream=stream)
+
     def run(self, stream=None):
-        """The whole step: write this step's K/V (slot mapping and scatter in one launch), then attend."""
-        self.write_kv_paged(stream)
-        self.decode(stream)
+        """The whole step: write this step's K/V, then attend (the decode tokens' K/V written by the decode
+        kernel itself when fused_decode_write)."""
+        self.write_stage(stream)
+        self.decode_stage(stream)
         self.prefill(stream)
         return self.out_decode, self.out_prefill
 

@@ -461,3 +461,23 @@ def test_multi_layer_pools_share_one_slot_mapping():
         want = oracle.decode(storage_numpy(q[layer]), kc, vc, w.block_tables.numpy()[:nd],
                              w.context_lens.numpy()[:nd], w.scale)
         assert _maxabs(got, want) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("name", ["decode_bf16", "mixed_bf16", "longctx_bf16"])
+def test_decode_write_equals_separate_write_then_decode(name):
+    """pa_decode_write (the decode kernel writes each sequence's newest token into the pool and attends with
+    it) leaves the same pools and slots as the separate write and gives the same outputs, bit for bit."""
+    w, exp = _case("small", name)
+    fused = DeviceStep(w)
+    assert fused.fused_decode_write
+    plain = DeviceStep(w, fused_decode_write=False)
+    fused.run()
+    plain.run()
+    torch.cuda.synchronize()
+    assert fused.errors() == 0 and plain.errors() == 0
+    assert torch.equal(fused.slots.cpu(), torch.from_numpy(exp.slots))
+    assert np.array_equal(storage_numpy(fused.k_cache.cpu()), exp.k_cache)
+    assert np.array_equal(storage_numpy(fused.v_cache.cpu()), exp.v_cache)
+    assert torch.equal(fused.out_decode, plain.out_decode)
+    assert torch.equal(fused.out_prefill, plain.out_prefill)
+    assert _maxabs(fused.out_decode, exp.out_decode) <= TOL[w.dtype]
