@@ -241,9 +241,16 @@ def oracle_step_time(w, target_seconds: float):
     while True:
         t0 = time.perf_counter()
         slots, _ = oracle.slot_mapping(bt, w.seq_idx.numpy(), w.pos.numpy(), w.block_size, w.num_blocks)
-        oracle.write_kv(args["kn"], args["vn"], kc, vc, slots)
         nd = w.num_decode
-        if nd:
+        if w.kv_fp8:  # quantising write, then attention over the pools read back in float64
+            oracle.write_kv_fp8(args["kn"], args["vn"], kc, vc, slots, w.k_scale, w.v_scale)
+            if nd:
+                oracle.decode(w.q_decode.double().numpy(), oracle.dequant_e4m3(kc, w.k_scale),
+                              oracle.dequant_e4m3(vc, w.v_scale), bt[:nd], w.context_lens.numpy()[:nd], w.scale,
+                              num_threads=threads)
+        else:
+            oracle.write_kv(args["kn"], args["vn"], kc, vc, slots)
+        if nd and not w.kv_fp8:
             oracle.decode(args["qd"], kc, vc, bt[:nd], w.context_lens.numpy()[:nd], w.scale, num_threads=threads)
         if w.num_chunks:
             oracle.prefill(args["qp"], w.cu_q_lens.numpy(), w.q_start_pos.numpy(), w.seq_of_chunk.numpy(), kc, vc, bt,
@@ -296,6 +303,8 @@ def workload_config(w, l2_flush: str = "write"):
     if shared:
         cfg["shared_prefix_seqs"] = shared
         cfg["groups"] = int(len(w.group_offsets) - 1)
+    if w.kv_fp8:
+        cfg["kv_pool"] = f"e4m3, k_scale {w.k_scale:g}, v_scale {w.v_scale:g}"
     return cfg
 
 
@@ -430,13 +439,16 @@ def run_native(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "dtype": "e4m3 KV, bf16 q" if w.kv_fp8 else "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
         "config": workload_config(w, args.l2_flush),
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
                      "kernel": ("pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; "
                                 "decode_merge_kernel)" if step.use_cascade
+                                else "pa_decode_fp8 (decode_tc_kernel over e4m3 pools + decode_merge_kernel)"
+                                if w.kv_fp8
                                 else "pa_decode_write (decode_tc_kernel with the decode tokens' KV write + "
                                      "decode_merge_kernel)" if step.fused_decode_write
                                 else "pa_decode (decode_tc_kernel + decode_merge_kernel)"),

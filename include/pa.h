@@ -128,6 +128,25 @@ PA_API int pa_write_kv_paged(const void* k_new, const void* v_new, int num_token
                              int32_t* error_count, void* stream);
 
 /*
+ * fp8 KV pools ("KV cache 显存管理…": the pool's size is layers x tokens x kv
+ * heads x head_dim x 2 x dtype_size; an e4m3 pool halves dtype_size).  The
+ * pools hold one e4m3 code per element (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities, largest finite 448) and read back as
+ * code * scale, one scale per pool.  This call is pa_write_kv_paged for such
+ * pools: every element x of the bf16 rows k_new / v_new ([num_tokens]
+ * [num_kv_heads][head_dim]) is stored as the e4m3 code nearest to
+ * x * (1.0f / scale) (float arithmetic; ties to the even code; magnitudes
+ * beyond 448 are held at 448), k_cache / v_cache being uint8
+ * [num_blocks][block_size][num_kv_heads][head_dim].  Scales must be finite
+ * and positive.
+ */
+PA_API int pa_write_kv_paged_fp8(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads,
+                                 int head_dim, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                                 const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                                 const int32_t* seq_idx, const int32_t* pos, int64_t* slot_mapping, float k_scale,
+                                 float v_scale, int32_t* error_count, void* stream);
+
+/*
  * Bytes of workspace pa_decode needs for these sizes (split-KV partial
  * results plus two work-queue counters).  Deterministic:
  * the same arguments on the same device always give the same size.
@@ -209,6 +228,23 @@ PA_API int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_h
                              const int32_t* context_lens, int max_context_len, const int32_t* group_offsets,
                              int num_groups, int max_group_size, const int32_t* prefix_lens, float scale,
                              void* workspace, size_t workspace_bytes, int32_t* error_count, void* stream);
+
+/*
+ * pa_decode over fp8 pools (see pa_write_kv_paged_fp8): k_cache / v_cache are
+ * uint8 [num_blocks][block_size][num_kv_heads][head_dim] e4m3 codes read back
+ * as code * k_scale and code * v_scale; q and out are bf16.  The same
+ * attention as pa_decode on the read-back values: the kernel loads half the
+ * bytes, converts the codes to f16 in registers and runs the products with
+ * f16 tensor-core MMAs (q * scale * log2(e) rounded to f16, so |q * scale|
+ * must stay below 4e4).  Workspace: pa_decode_workspace_size(...).  Supported:
+ * head_dim 128, num_q_heads/num_kv_heads <= 8, block_size 8, 16, 32 or 64;
+ * otherwise PA_ERR_UNSUPPORTED.
+ */
+PA_API int pa_decode_fp8(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+                         const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                         int max_context_len, float scale, float k_scale, float v_scale, void* workspace,
+                         size_t workspace_bytes, int32_t* error_count, void* stream);
 
 /*
  * pa_decode fused with the KV write of the step's decode tokens: sequence s's

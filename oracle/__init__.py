@@ -25,6 +25,7 @@ _LIB = os.path.join(_LIB_DIR, "liboracle.so")
 
 F32 = 0
 BF16 = 1
+F64 = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -53,6 +54,14 @@ def _load():
             lib.oracle_num_blocks.restype = i64
             lib.oracle_slot_mapping.argtypes = [i32p, i64, i64, i32p, i32p, i64, i64, i64, i64p]
             lib.oracle_map_to_kernel_blocks.argtypes = [i32p, i64, i64, i64, i32p, i64]
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_write_kv_fp8.argtypes = [vp, vp, i64, i64, i64, vp, vp, i64, i64, i64p, ctypes.c_float,
+                                                ctypes.c_float]
+            lib.oracle_dequant_e4m3.argtypes = [vp, i64, ctypes.c_float, dp]
+            lib.oracle_dequant_e4m3.restype = None
             lib.oracle_map_to_kernel_blocks.restype = None
             lib.oracle_slot_mapping.restype = ctypes.c_int
             lib.oracle_write_kv.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int, vp, vp, i64, i64, i64p]
@@ -77,7 +86,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"oracle storage dtype must be float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"oracle storage dtype must be float32, float64 or uint16 (bf16 bits), got {a.dtype}")
 
 
 def _threads(num_threads):
@@ -108,6 +119,38 @@ def map_to_kernel_blocks(mgr_tables, ratio: int, kernel_width: int | None = None
     out = np.empty((S, kw), dtype=np.int32)
     _load().oracle_map_to_kernel_blocks(mtp, S, W, int(ratio), out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                         kw)
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 code (NaN for the NaN codes)."""
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 code to float32 x (ties to even, saturating at 448)."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(x))))
+
+
+def write_kv_fp8(k_new, v_new, k_cache, v_cache, slots, k_scale: float, v_scale: float) -> int:
+    """Quantising write into uint8 e4m3 pools, in place: code = e4m3(x * (1/scale)); returns the error count."""
+    assert k_cache.dtype == v_cache.dtype == np.uint8 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    T, H, D = k_new.shape
+    P, B = k_cache.shape[0], k_cache.shape[1]
+    sl = np.ascontiguousarray(slots, dtype=np.int64)
+    rc = _load().oracle_write_kv_fp8(k_new.ctypes.data, v_new.ctypes.data, T, H, D, k_cache.ctypes.data,
+                                     v_cache.ctypes.data, P, B, sl.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                     float(k_scale), float(v_scale))
+    return -rc
+
+
+def dequant_e4m3(codes, scale: float) -> np.ndarray:
+    """codes * scale in float64 (exact)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_dequant_e4m3(c.ctypes.data, c.size, float(scale), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return out
 
 

@@ -28,7 +28,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
 
 /* [P2] §2.1 PagedAttention 核心原理 and [P3] "分页思想": a sequence of length L
  * needs ceil(L / B) logical blocks. */
@@ -41,6 +41,7 @@ int64_t oracle_num_blocks(int64_t seq_len, int64_t block_size) {
  * binary32 word, so the widening is exact. */
 static double load_elem(const void* base, int dtype, int64_t idx) {
     if (dtype == ORACLE_F32) return (double)((const float*)base)[idx];
+    if (dtype == ORACLE_F64) return ((const double*)base)[idx];
     uint16_t bits = ((const uint16_t*)base)[idx];
     uint32_t word = (uint32_t)bits << 16;
     float f;
@@ -48,7 +49,7 @@ static double load_elem(const void* base, int dtype, int64_t idx) {
     return (double)f;
 }
 
-static int elem_bytes(int dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+static int elem_bytes(int dtype) { return dtype == ORACLE_F32 ? 4 : dtype == ORACLE_F64 ? 8 : 2; }
 
 /* [P2] 代码实现部分 › "块表与槽位映射：BlockTable" (compute_slot_mapping) and
  * [P3] "PagedAttention 改变了什么": for the new token at position pos of
@@ -98,6 +99,70 @@ void oracle_map_to_kernel_blocks(const int32_t* mgr_tables, int64_t num_seqs, in
             kernel_tables[s * kernel_width + j] = entry;
         }
     }
+}
+
+/* ---- fp8 KV pools: the e4m3 format (1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448;
+ * exponent field 0 holds the subnormals m * 2^-9).  The pages give the pool
+ * formula with dtype_size as a free parameter ("KV cache 显存管理…", KV size
+ * formula); an fp8 pool stores code = e4m3(x / scale) per element with one
+ * scale per pool, and reads back code * scale. */
+
+/* Value of an e4m3 code, straight from the format's definition. */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = m * ldexp(1.0, -9);
+    else v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 code to x, ties to the even code, magnitudes beyond 448 held
+ * at 448 (saturating), NaN to NaN: a search over all 127 non-negative finite
+ * codes, so no bit manipulation has to be trusted. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    double a = fabs((double)x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    if (a > 448.0) best = 0x7E;
+    return (uint8_t)(best | (signbit(x) ? 0x80 : 0));
+}
+
+/* The fp8 pools' write: the slot-mapped copy of oracle_write_kv, each bf16
+ * element x stored as e4m3(x * (1.0f / scale)), the product and the
+ * reciprocal in float. */
+int oracle_write_kv_fp8(const uint16_t* k_new, const uint16_t* v_new, int64_t num_tokens, int64_t num_kv_heads,
+                        int64_t head_dim, uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks,
+                        int64_t block_size, const int64_t* slot_mapping, float k_scale, float v_scale) {
+    int errors = 0;
+    int64_t row = num_kv_heads * head_dim;
+    float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) { ++errors; continue; }
+        for (int64_t i = 0; i < row; ++i) {
+            float kx = (float)load_elem(k_new, ORACLE_BF16, t * row + i);
+            float vx = (float)load_elem(v_new, ORACLE_BF16, t * row + i);
+            k_cache[slot * row + i] = oracle_e4m3_encode(kx * k_inv);
+            v_cache[slot * row + i] = oracle_e4m3_encode(vx * v_inv);
+        }
+    }
+    return -errors;
+}
+
+/* code * scale for every element (exact in double: 4 + 24 significant bits). */
+void oracle_dequant_e4m3(const uint8_t* codes, int64_t n, float scale, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]) * (double)scale;
 }
 
 /* [P3] "对 ModelRunner 的影响": the slot tells where the current token's K/V is

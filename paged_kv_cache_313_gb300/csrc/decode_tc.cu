@@ -67,11 +67,14 @@ struct StageInfo {
     long long new_slot;  // and its pool slot
 };
 
-template <int D>
+// kFp8: the pools hold e4m3 codes (one byte per element) instead of bf16.
+template <int D, bool kFp8>
 struct TcCfg {
-    static constexpr int kHalves = D / 64;               // 64-column (128-byte) halves of a row
+    static constexpr int kRowBytes = kFp8 ? D : 2 * D;   // one token row of one kv head
+    static constexpr int kHalves = kRowBytes / 128;       // 128-byte segments (swizzle rows) of a token row
     static constexpr int kStageTok = 64;
-    static constexpr int kStages = D == 128 ? PA_DECODE_STAGES : 2 * PA_DECODE_STAGES;
+    // bf16 D=128: 32 KiB stages; bf16 D=64 and e4m3 D=128: 16 KiB stages, so more of them fit
+    static constexpr int kStages = kHalves == 2 ? PA_DECODE_STAGES : kFp8 ? 5 : 2 * PA_DECODE_STAGES;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kHalfBytes = kStageTok * 128;   // one half of a stage's K (or V) tile
@@ -83,7 +86,7 @@ struct TcCfg {
     static constexpr int kQ = kRing + kStages * kStageBytes;
     // pa_decode_write: the newest token's K and V rows of the item, staged next to each stage
     static constexpr int kNew = kQ + kStages * kQBytes;
-    static constexpr int kNewBytes = 2 * D * 2;
+    static constexpr int kNewBytes = kFp8 ? 0 : 2 * D * 2;  // (no fused write into e4m3 pools)
     static constexpr int kCum = kNew + kStages * kNewBytes;  // int [kMaxSeqs + 1]
     static constexpr int kInfo = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
@@ -125,11 +128,12 @@ __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int 
     kvh = r - split * Hkv;
 }
 
-template <int D>
-__global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
+template <int D, bool kFp8>
+__global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_SM)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeParams p, int* work) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, kFp8>;
+    static_assert(!kFp8 || D == 128, "fp8 pools: head_dim 128");
     constexpr int KT = D / 16;  // 16-wide k steps (QK^T) and m tiles (PV)
     const int N = p.num_seqs, Hkv = p.num_kv_heads, G = p.group, B = p.block_size;
 
@@ -357,7 +361,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
             o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         }
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*c4 and 2*c4+1
-        const float sl2 = p.scale_log2;
+        // base-2 score scale: fp8 pools fold the softmax scale into the f16 queries and the K scale here
+        const float sl2 = kFp8 ? p.k_scale : p.scale_log2;
         int item_parity = 0;
         const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kHalves * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
@@ -379,6 +384,24 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 for (int kk = 0; kk < KT; ++kk) {
                     qb[kk][0] = row_ok ? __ldg(qg + kk * 8 + c4) : 0u;
                     qb[kk][1] = row_ok ? __ldg(qg + kk * 8 + c4 + 4) : 0u;
+                }
+            } else if ((inf.flags & 1) && kFp8) {
+                // fp8 pools: q * scale * log2(e) as f16, in the k order the e4m3 K fragments arrive in
+                // (lane (g4, c4) of the 32-column group kq holds columns 4c4..4c4+3 and 16+4c4..16+4c4+3:
+                // fragment 2kq takes the first two of each four, fragment 2kq+1 the last two)
+                const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(smem + C::kQ + slot * C::kQBytes);
+                const float qsc = p.scale_log2;
+#pragma unroll
+                for (int kk = 0; kk < KT; ++kk) {
+                    const int base = (kk >> 1) * 32 + 4 * c4 + (kk & 1) * 2;
+                    if (g4 < G) {
+                        const __nv_bfloat16* r = qs + g4 * D;
+                        qb[kk][0] = pack_f16x2(__bfloat162float(r[base]) * qsc, __bfloat162float(r[base + 1]) * qsc);
+                        qb[kk][1] = pack_f16x2(__bfloat162float(r[base + 16]) * qsc,
+                                               __bfloat162float(r[base + 17]) * qsc);
+                    } else {
+                        qb[kk][0] = qb[kk][1] = 0u;
+                    }
                 }
             } else if (inf.flags & 1) {  // first stage of an item: load its queries
                 const uint8_t* qs = smem + C::kQ + slot * C::kQBytes;
@@ -417,7 +440,23 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 }
                 // S^T = K Q^T (two independent accumulation chains)
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-                {
+                if constexpr (kFp8) {
+                    // one ldmatrix.x4 per 32 e4m3 columns: each register holds four consecutive codes of a row,
+                    // the low two feeding fragment 2kq and the high two fragment 2kq+1 (f16 after conversion)
+                    const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+                    for (int kq = 0; kq < D / 32; ++kq) {
+                        uint32_t raw[4], a[4];
+                        ldmatrix_x4(raw, kbase + tr.at(r, 0, 2 * kq + (lane >> 4)));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
+                        mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] >> 16);
+                        mma_f16_16816(sb, a, qb[2 * kq + 1][0], qb[2 * kq + 1][1]);
+                    }
+                } else {
                     const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
                     const uint32_t kbase = smem_u32(kt);
 #pragma unroll
@@ -458,9 +497,28 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                     o[mt][2] *= a0;
                     o[mt][3] *= a1;
                 }
-                const uint32_t b0 = movmatrix_trans(pack_bf16x2(p0, p1));
-                const uint32_t b1 = movmatrix_trans(pack_bf16x2(p2, p3));
-                {  // O^T += V^T P^T
+                const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+                const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+                if constexpr (kFp8) {
+                    // O^T += V^T P^T: ldmatrix.trans of 16-bit pairs gives a lane the codes of tokens 2c4 and
+                    // 2c4+1 at columns 2g4 and 2g4+1; a byte permutation regroups them per column, so
+                    // fragment 2kv holds the even columns of the 32-column group kv and 2kv+1 the odd ones
+                    const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
+                    const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+                    for (int kv = 0; kv < D / 32; ++kv) {
+                        uint32_t raw[4], ev[4], od[4];
+                        ldmatrix_x4_trans(raw, vbase + tr.at(r, 0, 2 * kv + ((lane >> 3) & 1)));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
+                            ev[i] = e4m3x2_to_f16x2(t & 0xFFFFu);
+                            od[i] = e4m3x2_to_f16x2(t >> 16);
+                        }
+                        mma_f16_16816(o[2 * kv], ev, b0, b1);
+                        mma_f16_16816(o[2 * kv + 1], od, b0, b1);
+                    }
+                } else {  // O^T += V^T P^T
                     const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
                     const uint32_t vbase = smem_u32(vt);
 #pragma unroll
@@ -575,11 +633,13 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 float* my = slabs + warp * 8 * D;
 #pragma unroll
                 for (int mt = 0; mt < KT; ++mt) {
-                    const int d = mt * 16 + g4;
-                    my[(2 * c4) * D + d] = o[mt][0] * f0;
-                    my[(2 * c4 + 1) * D + d] = o[mt][1] * f1;
-                    my[(2 * c4) * D + d + 8] = o[mt][2] * f0;
-                    my[(2 * c4 + 1) * D + d + 8] = o[mt][3] * f1;
+                    // the output columns of fragment mt (fp8: even / odd columns of a 32-column group)
+                    const int d0 = kFp8 ? (mt >> 1) * 32 + 2 * g4 + (mt & 1) : mt * 16 + g4;
+                    const int d1 = kFp8 ? d0 + 16 : d0 + 8;
+                    my[(2 * c4) * D + d0] = o[mt][0] * f0;
+                    my[(2 * c4 + 1) * D + d0] = o[mt][1] * f1;
+                    my[(2 * c4) * D + d1] = o[mt][2] * f0;
+                    my[(2 * c4 + 1) * D + d1] = o[mt][3] * f1;
                 }
             }
             fence_proxy_async_smem();  // these writes precede the slot's next TMA write
@@ -603,7 +663,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
                 float acc = slabs[idx];
 #pragma unroll
                 for (int w = 1; w < C::kConsumerWarps; ++w) acc += slabs[w * 8 * D + idx];
-                const float val = Ls > 0.f ? acc / Ls : 0.f;
+                const float val = Ls > 0.f ? acc / Ls * (kFp8 ? p.v_scale : 1.f) : 0.f;
                 if (inf.flags & 4) {
                     out[idx] = __float2bfloat16_rn(val);
                 } else {
@@ -627,21 +687,22 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, PA_DECODE_CTAS_PER_SM)
     }
 }
 
-template <int D>
+template <int D, bool kFp8>
 int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, kFp8>;
     CUtensorMap tmk, tmv;
-    int rc = pool_tensor_map_rows(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D);
+    int rc = pool_tensor_map_rows(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8);
     if (rc != PA_OK) return rc;
-    if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D)) != PA_OK) return rc;
-    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D>), C::kSmemBytes)) != PA_OK)
+    if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8)) != PA_OK)
+        return rc;
+    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8>), C::kSmemBytes)) != PA_OK)
         return rc;
     // PA_DECODE_CTAS_PER_SM CTAs per SM, never more CTAs than the largest possible item count
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * PA_DECODE_CTAS_PER_SM;
     int grid = (int)(max_items < slots ? max_items : slots);
-    return launch_kernel(decode_tc_kernel<D>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv, p,
-                         p.work);
+    return launch_kernel(decode_tc_kernel<D, kFp8>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv,
+                         p, p.work);
 }
 
 }  // namespace
@@ -679,14 +740,17 @@ int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int bloc
 // (0, pb*B, kvh*D/64) is block pb's B rows of kv head kvh, stored
 // [segment][row][64] and 128-byte swizzled.
 int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                         int head_dim) {
+                         int head_dim, bool fp8) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
-    cuuint64_t dims[3] = {64, (cuuint64_t)num_blocks * block_size, (cuuint64_t)num_kv_heads * head_dim / 64};
-    cuuint64_t strides[2] = {(cuuint64_t)num_kv_heads * head_dim * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)block_size, (cuuint32_t)(head_dim / 64)};
+    // x: elements of one 128-byte segment; the segments of a row are 128 bytes apart
+    const int esz = fp8 ? 1 : 2, seg = 128 / esz, row_bytes = num_kv_heads * head_dim * esz;
+    cuuint64_t dims[3] = {(cuuint64_t)seg, (cuuint64_t)num_blocks * block_size, (cuuint64_t)row_bytes / 128};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
+    cuuint32_t box[3] = {(cuuint32_t)seg, (cuuint32_t)block_size, (cuuint32_t)(head_dim * esz / 128)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
+    CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void*>(pool), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
@@ -695,6 +759,8 @@ int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int
 bool decode_tc_supported(const DecodeParams& p, int dtype) {
     const int B = p.block_size;
     if (dtype != PA_BF16 || (p.head_dim != 64 && p.head_dim != 128) || p.group > 8) return false;
+    // fp8 pools: head_dim 128, plain decode (no cascade items, no fused write)
+    if (p.kv_fp8 && (p.head_dim != 128 || p.group_offsets || p.k_new)) return false;
     if (B != 8 && B != 16 && B != 32 && B != 64) return false;
     if (p.partition % 64 != 0 || p.num_seqs > kMaxSeqsPersistent) return false;
     if (((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) || ((uintptr_t)p.q & 15)) return false;
@@ -703,7 +769,8 @@ bool decode_tc_supported(const DecodeParams& p, int dtype) {
 }
 
 int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-    return p.head_dim == 64 ? launch<64>(p, num_sms, stream) : launch<128>(p, num_sms, stream);
+    if (p.kv_fp8) return launch<128, true>(p, num_sms, stream);
+    return p.head_dim == 64 ? launch<64, false>(p, num_sms, stream) : launch<128, false>(p, num_sms, stream);
 }
 
 }  // namespace pa

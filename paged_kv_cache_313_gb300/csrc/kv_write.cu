@@ -105,6 +105,53 @@ __global__ void write_kv_kernel(const int4* __restrict__ k_new, const int4* __re
     }
 }
 
+// Two floats to their nearest e4m3 codes (ties to even, saturating at 448),
+// packed as {lo: byte 0, hi: byte 1}.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// pa_write_kv_paged_fp8: slot mapping, then each bf16 element x of the token's
+// K and V rows stored as e4m3(x * inv_scale) into uint8 pools.  One CTA per
+// token; a thread converts eight elements (16 bytes in, 8 bytes out).
+__global__ void write_kv_paged_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                          int row_vec8, uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
+                                          const int32_t* __restrict__ block_tables, int num_seqs,
+                                          int max_blocks_per_seq, const int32_t* __restrict__ seq_idx,
+                                          const int32_t* __restrict__ pos, int block_size, int num_blocks,
+                                          int64_t* __restrict__ slots, float k_inv, float v_inv,
+                                          int32_t* error_count) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ long long s_slot;
+    const int t = blockIdx.x;
+    if (threadIdx.x == 0) {
+        s_slot = slot_of(block_tables, num_seqs, max_blocks_per_seq, seq_idx, pos, t, block_size, num_blocks,
+                         error_count);
+        if (slots) slots[t] = s_slot;
+    }
+    __syncthreads();
+    const long long slot = s_slot;
+    if (slot < 0) return;
+    for (int i = threadIdx.x; i < 2 * row_vec8; i += blockDim.x) {
+        const bool isv = i >= row_vec8;
+        const int j = isv ? i - row_vec8 : i;
+        const uint4 x = isv ? __ldg(v_new + (long long)t * row_vec8 + j) : __ldg(k_new + (long long)t * row_vec8 + j);
+        const float inv = isv ? v_inv : k_inv;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint16_t q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+            q[k] = pack_e4m3x2(__fmul_rn(lo, inv), __fmul_rn(hi, inv));
+        }
+        const uint2 out = make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+        (isv ? v_cache : k_cache)[slot * row_vec8 + j] = out;
+    }
+}
+
 // One CTA per copy: num_valid token rows of the source block, both pools.
 __global__ void copy_blocks_kernel(int4* __restrict__ k_cache, int4* __restrict__ v_cache, int num_blocks,
                                    int block_size, int row_vecs, const int32_t* __restrict__ src,
@@ -160,6 +207,20 @@ int launch_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, 
                          static_cast<const int4*>(k_new), static_cast<const int4*>(v_new), row_vecs,
                          static_cast<int4*>(k_cache), static_cast<int4*>(v_cache), block_tables, num_seqs,
                          max_blocks_per_seq, seq_idx, pos, block_size, num_blocks, slot_mapping, error_count);
+}
+
+int launch_write_kv_paged_fp8(const void* k_new, const void* v_new, int num_tokens, int row_elems, void* k_cache,
+                              void* v_cache, const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                              const int32_t* seq_idx, const int32_t* pos, int block_size, int num_blocks,
+                              int64_t* slot_mapping, float k_inv, float v_inv, int32_t* error_count,
+                              cudaStream_t stream) {
+    const int row_vec8 = row_elems / 8;
+    const int threads = 2 * row_vec8 >= 256 ? 256 : ((2 * row_vec8 + 31) / 32) * 32;
+    return launch_kernel(write_kv_paged_fp8_kernel, dim3(num_tokens), dim3(threads), 0, stream,
+                         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), row_vec8,
+                         static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), block_tables, num_seqs,
+                         max_blocks_per_seq, seq_idx, pos, block_size, num_blocks, slot_mapping, k_inv, v_inv,
+                         error_count);
 }
 
 int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,

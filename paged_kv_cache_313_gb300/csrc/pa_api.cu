@@ -1,6 +1,7 @@
 // pa_api.cu — the C ABI of libpa.so: argument checks, device checks and
 // dispatch to the kernels.  Every entry point validates on the host and
 // launches nothing when a check fails.
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -202,6 +203,31 @@ int pa_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, int 
                                  static_cast<cudaStream_t>(stream));
 }
 
+int pa_write_kv_paged_fp8(const void* k_new, const void* v_new, int num_tokens, int num_kv_heads, int head_dim,
+                          void* k_cache, void* v_cache, int num_blocks, int block_size, const int32_t* block_tables,
+                          int num_seqs, int max_blocks_per_seq, const int32_t* seq_idx, const int32_t* pos,
+                          int64_t* slot_mapping, float k_scale, float v_scale, int32_t* error_count, void* stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || num_blocks < 0 || block_size < 1 || num_seqs < 0 ||
+        max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !seq_idx || !pos ||
+        (num_seqs > 0 && max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_INVALID_ARG;
+    const long long row = (long long)num_kv_heads * head_dim;  // elements; fp8 row bytes = row
+    if (row % 16 != 0 || row > (1 << 20)) return PA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_UNSUPPORTED;
+    int rc = check_device(nullptr);
+    if (rc != PA_OK) return rc;
+    const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+    return launch_write_kv_paged_fp8(k_new, v_new, num_tokens, (int)row, k_cache, v_cache, block_tables, num_seqs,
+                                     max_blocks_per_seq, seq_idx, pos, block_size, num_blocks, slot_mapping, k_inv,
+                                     v_inv, error_count, static_cast<cudaStream_t>(stream));
+}
+
 int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int num_kv_heads, int head_dim,
                    int dtype, const int32_t* src_blocks, const int32_t* dst_blocks, const int32_t* num_valid,
                    int num_copies, int32_t* error_count, void* stream) {
@@ -309,6 +335,28 @@ int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_k
                             max_context_len, scale, workspace, workspace_bytes, error_count);
     if (rc != PA_OK) return rc;
     return run_decode(p, dtype, num_sms, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_fp8(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                  const void* k_cache, const void* v_cache, int num_blocks, int block_size,
+                  const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                  int max_context_len, float scale, float k_scale, float v_scale, void* workspace,
+                  size_t workspace_bytes, int32_t* error_count, void* stream) {
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 && num_blocks >= 0 && max_blocks_per_seq >= 0 && max_context_len >= 0 &&
+        decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size) == PA_OK)
+        return PA_OK;
+    DecodeParams p;
+    int num_sms = 0;
+    int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, PA_BF16, k_cache,
+                            v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, scale, workspace, workspace_bytes, error_count);
+    if (rc != PA_OK) return rc;
+    p.kv_fp8 = 1;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    if (!decode_tc_supported(p, PA_BF16)) return PA_ERR_UNSUPPORTED;
+    return run_decode(p, PA_BF16, num_sms, static_cast<cudaStream_t>(stream));
 }
 
 int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,

@@ -97,6 +97,9 @@ struct DecodeParams {
     void* k_write = nullptr;
     void* v_write = nullptr;
     int64_t* new_slots = nullptr;
+    // fp8 pools: k_cache / v_cache hold e4m3 codes read back as code * k_scale / code * v_scale
+    int kv_fp8 = 0;
+    float k_scale = 1.f, v_scale = 1.f;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;
@@ -143,6 +146,11 @@ int launch_write_kv_paged(const void* k_new, const void* v_new, int num_tokens, 
                           void* v_cache, const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
                           const int32_t* seq_idx, const int32_t* pos, int block_size, int num_blocks,
                           int64_t* slot_mapping, int32_t* error_count, cudaStream_t stream);
+int launch_write_kv_paged_fp8(const void* k_new, const void* v_new, int num_tokens, int row_elems, void* k_cache,
+                              void* v_cache, const int32_t* block_tables, int num_seqs, int max_blocks_per_seq,
+                              const int32_t* seq_idx, const int32_t* pos, int block_size, int num_blocks,
+                              int64_t* slot_mapping, float k_inv, float v_inv, int32_t* error_count,
+                              cudaStream_t stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size, int row_bytes,
                        const int32_t* src, const int32_t* dst, const int32_t* num_valid, int num_copies,
                        int32_t* error_count, cudaStream_t stream);

@@ -18,10 +18,11 @@ namespace pa {
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
                     int head_dim);
-// The same pool as a 3-D map whose box {64, B, D/64} is one block's B rows of
-// one kv head, both 64-column halves ([half][row][64] in shared memory).
+// The same pool as a 3-D map whose box is one block's B rows of one kv head,
+// every 128-byte segment of the row ([segment][row][128 bytes] in shared
+// memory): {64, B, D/64} for bf16, {128, B, D/128} for e4m3 pools.
 int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                         int head_dim);
+                         int head_dim, bool fp8 = false);
 
 constexpr uint32_t kSpinLimit = 1u << 18;
 
@@ -129,6 +130,30 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low byte, high byte) to two f16 (low half, high half); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+    uint32_t d;
+    const uint16_t c = (uint16_t)codes16;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(c));
+    return d;
+}
+
+// Two floats to an f16x2 word (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -19,7 +19,7 @@ PA_F32, PA_BF16 = 0, 1
 
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
-           "pa_write_kv_paged", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_write",
+           "pa_write_kv_paged", "pa_write_kv_paged_fp8", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_fp8", "pa_decode_write",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
            "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy")
 
@@ -42,9 +42,11 @@ _SIGNATURES = {
     "pa_slot_mapping": ([_p, _i, _i, _p, _p, _i, _i, _i, _p, _p, _p], _i),
     "pa_write_kv": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _p, _p], _i),
     "pa_write_kv_paged": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _i, _p, _p, _p, _p, _p], _i),
+    "pa_write_kv_paged_fp8": ([_p, _p, _i, _i, _i, _p, _p, _i, _i, _p, _i, _i, _p, _p, _p, _f, _f, _p, _p], _i),
     "pa_decode_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
+    "pa_decode_fp8": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _f, _f, _p, _sz, _p, _p], _i),
     "pa_decode_write": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p, _p, _p, _sz, _p,
                          _p], _i),
     "pa_decode_cascade_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
@@ -166,6 +168,23 @@ def pa_write_kv_paged(k_new, v_new, k_cache, v_cache, block_tables, seq_idx, pos
     return slot_mapping
 
 
+def pa_write_kv_paged_fp8(k_new, v_new, k_cache, v_cache, block_tables, seq_idx, pos, k_scale: float,
+                          v_scale: float, slot_mapping=None, error_count=None, stream=None):
+    """Slot mapping and a quantising K/V write into uint8 e4m3 pools (code = e4m3(x / scale))."""
+    T, H, D = k_new.shape
+    P, B = k_cache.shape[0], k_cache.shape[1]
+    S, W = block_tables.shape
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("fp8 pools are uint8 tensors of e4m3 codes")
+    _check("pa_write_kv_paged_fp8", lib().pa_write_kv_paged_fp8(
+        _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16), T, H, D,
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), P, B, _dev(block_tables, "block_tables", torch.int32),
+        S, W, _dev(seq_idx, "seq_idx", torch.int32), _dev(pos, "pos", torch.int32),
+        _dev(slot_mapping, "slot_mapping", torch.int64), float(k_scale), float(v_scale),
+        _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return slot_mapping
+
+
 def pa_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len):
     """(partition length in tokens, number of partitions) pa_decode uses for these sizes."""
     part, splits = ctypes.c_int(0), ctypes.c_int(0)
@@ -197,6 +216,26 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return out
+
+
+def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                  k_scale: float, v_scale: float, workspace, out=None, error_count=None, stream=None) -> torch.Tensor:
+    """pa_decode over uint8 e4m3 pools read back as code * scale; q and out bf16."""
+    N, Hq, D = q.shape
+    P, B, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_cache differ")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("fp8 pools are uint8 tensors of e4m3 codes")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode_fp8", lib().pa_decode_fp8(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), N, Hq, Hkv, D, _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), P, B, _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale), float(k_scale),
+        float(v_scale), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
     return out
 

@@ -68,7 +68,10 @@ class DeviceStep:
         self.workspace = (pa.new_decode_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                                   self.max_context_len, device=dev) if nd else None)
         # cascade decode when decode sequences share prefixes (and the shapes allow it)
-        self.use_cascade = bool(cascade and nd and int(w.prefix_lens.max()) > 0 and w.dtype == torch.bfloat16
+        if w.kv_fp8 and w.num_chunks:
+            raise ValueError("e4m3 pools are read by decode only; prefill chunks need bf16 or fp32 pools")
+        self.use_cascade = bool(cascade and nd and not w.kv_fp8 and int(w.prefix_lens.max()) > 0
+                                and w.dtype == torch.bfloat16
                                 and w.head_dim == 128 and w.num_q_heads // w.num_kv_heads in (1, 2, 4, 8)
                                 and w.block_size in (8, 16, 32, 64))
         self.cascade_workspace = (pa.new_cascade_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -79,7 +82,7 @@ class DeviceStep:
         G = w.num_q_heads // w.num_kv_heads
         newest = bool(nd) and torch.equal(w.seq_idx[:nd], torch.arange(nd, dtype=w.seq_idx.dtype)) and \
             torch.equal(w.pos[:nd], w.context_lens[:nd].to(w.pos.dtype) - 1)
-        self.fused_decode_write = bool(fused_decode_write and newest and not self.use_cascade
+        self.fused_decode_write = bool(fused_decode_write and newest and not self.use_cascade and not w.kv_fp8
                                        and w.dtype == torch.bfloat16 and w.head_dim in (64, 128) and G <= 8
                                        and w.block_size in (8, 16, 32, 64))
         n = pa.pa_prefill_workspace_size(w.num_chunks, w.max_q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -98,6 +101,11 @@ class DeviceStep:
 
     def write_kv_paged(self, stream=None):
         """Slot mapping and K/V write in one launch (the slots are still recorded)."""
+        if self.w.kv_fp8:
+            pa.pa_write_kv_paged_fp8(self.k_new, self.v_new, self.k_cache, self.v_cache, self.block_tables,
+                                     self.seq_idx, self.pos, self.w.k_scale, self.w.v_scale, slot_mapping=self.slots,
+                                     error_count=self.error_count, stream=stream)
+            return
         pa.pa_write_kv_paged(self.k_new, self.v_new, self.k_cache, self.v_cache, self.block_tables, self.seq_idx,
                              self.pos, slot_mapping=self.slots, error_count=self.error_count, stream=stream)
 
@@ -106,6 +114,11 @@ class DeviceStep:
         if not w.num_decode:
             return self.out_decode
         nd = w.num_decode
+        if w.kv_fp8:
+            return pa.pa_decode_fp8(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
+                                    self.context_lens[:nd], self.max_context_len, w.scale, w.k_scale, w.v_scale,
+                                    self.workspace, out=self.out_decode, error_count=self.error_count,
+                                    stream=stream)
         if self.use_cascade:
             return pa.pa_decode_cascade(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
                                         self.context_lens[:nd], self.max_context_len, self.group_offsets,

@@ -62,6 +62,10 @@ class Workload:
     group_offsets: torch.Tensor | None = None  # int32 [G+1]
     prefix_lens: torch.Tensor | None = None  # int32 [num_decode]
     max_group_size: int = 0
+    # e4m3 pools (uint8 codes read back as code * scale); q, new K/V and outputs stay bf16
+    kv_fp8: bool = False
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def num_seqs(self) -> int:
@@ -89,7 +93,7 @@ class Workload:
 
     def kv_bytes_per_token(self) -> int:
         """K and V bytes of one token across all KV heads (one layer)."""
-        return 2 * self.num_kv_heads * self.head_dim * self.elem_bytes
+        return 2 * self.num_kv_heads * self.head_dim * (1 if self.kv_fp8 else self.elem_bytes)
 
 
 def _normal(rng: np.random.Generator, shape, dtype: torch.dtype) -> torch.Tensor:
@@ -204,6 +208,28 @@ def shared_prefix_bf16(seed: int = 0, num_prompts: int = 32, branches: int = 8, 
     return _finish(name, torch.bfloat16, 32, 8, 128, B, alloc, vrng, seqs, lens, cow=cow, meta=meta)
 
 
+def as_fp8(w: Workload, seed: int, k_scale: float = 1.0 / 64, v_scale: float = 1.0 / 64, lo: int = 0x30,
+           hi: int = 0x60) -> Workload:
+    """The same batch over e4m3 pools: every pool byte becomes a random code whose low seven bits are drawn
+    from [lo, hi) (0x30..0x5f: exponent fields 6..11, magnitudes 0.25..60 before the scale; hi <= 0x7f keeps
+    NaN codes out) with a random sign.  Queries and the new tokens' K/V stay bf16."""
+    rng = np.random.default_rng(seed + 5000)
+    shape = tuple(w.k_cache.shape)
+    codes = lambda: torch.from_numpy(rng.integers(lo, hi, size=shape, dtype=np.uint8) |  # noqa: E731
+                                     (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7))
+    w.k_cache, w.v_cache = codes(), codes()
+    w.kv_fp8, w.k_scale, w.v_scale = True, float(k_scale), float(v_scale)
+    return w
+
+
+def decode_fp8(seed: int = 0, num_seqs: int = 64, min_len: int = 128, max_len: int = 4096) -> Workload:
+    """The bf16 decode workload's batch (64 sequences, lengths U[128, 4096], 32/8 heads, D=128, B=16) over e4m3
+    pools (history codes as in ``as_fp8``, k_scale = v_scale = 1/64)."""
+    w = as_fp8(decode_bf16(seed, num_seqs, min_len, max_len), seed)
+    w.name = "decode_fp8"
+    return w
+
+
 def shared_prefix_cow_bf16(seed: int = 0) -> Workload:
     """Correctness variant of the shared-prefix workload whose 2050-token prefix
     ends two tokens into a block, so the branches' first writes copy it."""
@@ -275,13 +301,15 @@ def small(name: str, seed: int = 0) -> Workload:
         return mixed_bf16(seed, num_decode=12, num_chunks=3, chunk_len=200, max_off=500)
     if name == "tiny_fp32":
         return tiny_fp32(seed)
+    if name == "decode_fp8":
+        return decode_fp8(seed, num_seqs=12, min_len=1, max_len=700)
     raise KeyError(name)
 
 
 def make(name: str, seed: int = 0) -> Workload:
     return {"tiny_fp32": tiny_fp32, "decode_bf16": decode_bf16, "longctx_bf16": longctx_bf16,
             "shared_prefix_bf16": shared_prefix_bf16, "shared_prefix_cow_bf16": shared_prefix_cow_bf16,
-            "mixed_bf16": mixed_bf16}[name](seed)
+            "mixed_bf16": mixed_bf16, "decode_fp8": decode_fp8}[name](seed)
 
 
 def storage_numpy(t: torch.Tensor) -> np.ndarray:

@@ -37,9 +37,10 @@ def _case(kind, name):
     return _cache[key]
 
 
-CASES = [("small", n) for n in ("tiny_fp32", "decode_bf16", "longctx_bf16", "shared_prefix_bf16", "mixed_bf16")] + \
+CASES = [("small", n) for n in ("tiny_fp32", "decode_bf16", "longctx_bf16", "shared_prefix_bf16", "mixed_bf16",
+                                 "decode_fp8")] + \
         [("full", n) for n in ("decode_bf16", "longctx_bf16", "shared_prefix_bf16", "shared_prefix_cow_bf16",
-                               "mixed_bf16")]
+                               "mixed_bf16", "decode_fp8")]
 
 
 def _maxabs(got: torch.Tensor, want: np.ndarray) -> float:
@@ -52,9 +53,13 @@ def _maxabs(got: torch.Tensor, want: np.ndarray) -> float:
 def test_step_parity(kind, name):
     w, exp = _case(kind, name)
     st = DeviceStep(w)
-    st.slot_mapping()
+    if w.kv_fp8:
+        st.write_kv_paged()  # the quantising write maps the slots itself and records them
+    else:
+        st.slot_mapping()
     assert torch.equal(st.slots.cpu(), torch.from_numpy(exp.slots)), "slot mapping differs"
-    st.write_kv()
+    if not w.kv_fp8:
+        st.write_kv()
     kc = storage_numpy(st.k_cache.cpu())
     vc = storage_numpy(st.v_cache.cpu())
     assert np.array_equal(kc, exp.k_cache) and np.array_equal(vc, exp.v_cache), "pool contents differ after write"
@@ -481,3 +486,69 @@ def test_decode_write_equals_separate_write_then_decode(name):
     assert torch.equal(fused.out_decode, plain.out_decode)
     assert torch.equal(fused.out_prefill, plain.out_prefill)
     assert _maxabs(fused.out_decode, exp.out_decode) <= TOL[w.dtype]
+
+
+# ---- e4m3 pools ------------------------------------------------------------
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 0.37), (1.0 / 64, 3.0)])
+def test_fp8_write_of_every_bf16_value_matches_oracle(k_scale, v_scale):
+    """The quantising write, bit-exact against the oracle's nearest-code search, for every bf16 bit pattern but
+    the NaNs (64 tokens x 8 heads x 128 = 65536 elements; infinities saturate), at power-of-two scales and at
+    scales whose reciprocal and product round; whole pools compared, untouched slots included."""
+    T, H, D, B, P = 64, 8, 128, 16, 9
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    bits[((bits & 0x7F80) == 0x7F80) & ((bits & 0x7F) != 0)] = 0
+    rng = np.random.default_rng(11)
+    k_bits = bits.reshape(T, H, D)
+    v_bits = rng.permutation(bits).reshape(T, H, D)
+    bt = np.array([[7, 2, 5, 0]], dtype=np.int32)
+    seq_idx = np.zeros(T, dtype=np.int32)
+    pos = np.arange(T, dtype=np.int32)
+    kc0 = rng.integers(0, 256, size=(P, B, H, D), dtype=np.uint8)
+    vc0 = rng.integers(0, 256, size=(P, B, H, D), dtype=np.uint8)
+    slots, nerr = oracle.slot_mapping(bt, seq_idx, pos, B, P)
+    assert nerr == 0
+    k_exp, v_exp = kc0.copy(), vc0.copy()
+    assert oracle.write_kv_fp8(k_bits, v_bits, k_exp, v_exp, slots, k_scale, v_scale) == 0
+
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    bf = lambda b: dev(b.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    kc, vc = dev(kc0), dev(vc0)
+    slot_out = torch.empty(T, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv_paged_fp8(bf(k_bits), bf(v_bits), kc, vc, dev(bt), dev(seq_idx), dev(pos), k_scale, v_scale,
+                             slot_mapping=slot_out, error_count=err)
+    torch.cuda.synchronize()
+    assert torch.equal(slot_out.cpu(), torch.from_numpy(slots))
+    assert np.array_equal(kc.cpu().numpy(), k_exp), "K codes differ"
+    assert np.array_equal(vc.cpu().numpy(), v_exp), "V codes differ"
+    assert int(err.item()) == 0
+
+
+FP8_DECODE_CASES = [
+    # (Hq, Hkv, B, decode context lengths, code range): every block size, groups 1..8, partition boundaries,
+    # and codes over the whole finite range (subnormals up to 448) through the in-register conversion
+    (8, 8, 8, [1, 63, 64, 65, 700], (0x30, 0x60)),
+    (16, 8, 16, [5, 512, 513, 2000], (0x30, 0x60)),
+    (32, 8, 32, [3000, 17, 129], (0x30, 0x60)),
+    (64, 8, 64, [1, 100, 4097], (0x30, 0x60)),
+    (32, 8, 16, [900, 64, 1], (0x00, 0x7F)),
+    (16, 2, 8, [1025, 64], (0x00, 0x7F)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FP8_DECODE_CASES)))
+def test_fp8_decode_shapes(case):
+    Hq, Hkv, B, lens, (lo, hi) = FP8_DECODE_CASES[case]
+    w = W.prefill_batch(300 + case, Hq, Hkv, 128, B, [], [], dtype=torch.bfloat16, decode_lens=lens)
+    ks, vs = (1.0 / 64, 1.0 / 64) if hi <= 0x60 else (1.0 / 256, 1.0 / 128)
+    W.as_fp8(w, 300 + case, ks, vs, lo, hi)
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(storage_numpy(st.k_cache.cpu()), exp.k_cache)
+    assert np.array_equal(storage_numpy(st.v_cache.cpu()), exp.v_cache)
+    err = _maxabs(st.out_decode, exp.out_decode)
+    assert err <= TOL[torch.bfloat16], f"fp8 decode max-abs error {err}"
+    assert st.errors() == 0

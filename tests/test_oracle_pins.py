@@ -344,3 +344,53 @@ def test_map_to_kernel_blocks_keeps_every_slot():
         s_ker, e2 = oracle.slot_mapping(kern, seq, pos, Bk, P * ratio)
         assert e1 == e2 == 0
         assert np.array_equal(s_mgr, s_ker)
+
+
+# ---- fp8 (e4m3) pools: the oracle's format against the format's defining values
+
+def test_e4m3_defining_values():
+    assert oracle.e4m3_value(0x00) == 0.0
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9  # smallest subnormal
+    assert oracle.e4m3_value(0x07) == 7 * 2.0 ** -9  # largest subnormal
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6  # smallest normal
+    assert oracle.e4m3_value(0x38) == 1.0
+    assert oracle.e4m3_value(0x3C) == 1.5
+    assert oracle.e4m3_value(0x7E) == 448.0  # largest finite
+    assert np.isnan(oracle.e4m3_value(0x7F)) and np.isnan(oracle.e4m3_value(0xFF))
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(b > a for a, b in zip(vals, vals[1:]))  # strictly increasing over the finite codes
+    for c in range(0x7F):
+        assert oracle.e4m3_value(c | 0x80) == -vals[c] or (c == 0 and np.signbit(oracle.e4m3_value(0x80)))
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    for c in range(0x7F):
+        v = oracle.e4m3_value(c)
+        assert oracle.e4m3_encode(v) == c and oracle.e4m3_encode(-v) == (c | 0x80)
+    for c in range(0x7E):  # midpoints go to the code with an even mantissa
+        mid = (oracle.e4m3_value(c) + oracle.e4m3_value(c + 1)) / 2
+        if np.float32(mid) == mid:
+            assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1)
+    assert oracle.e4m3_encode(449.0) == 0x7E and oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(-500.0) == 0xFE
+    rng = np.random.default_rng(3)
+    finite = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    for x in rng.standard_normal(300).astype(np.float32) * 40:
+        got = oracle.e4m3_value(oracle.e4m3_encode(x))
+        assert abs(abs(x) - abs(got)) <= np.abs(finite - abs(x)).min() + 1e-12  # a nearest code
+
+
+def test_fp8_write_round_trips_representable_values():
+    """Values that are exactly code * scale come back exactly through the quantising write."""
+    import torch
+    scale = 0.03125  # a power of two: x * (1 / scale) is exact
+    codes = np.arange(0, 0x7F, dtype=np.uint8)
+    vals = np.array([oracle.e4m3_value(c) * scale for c in codes], dtype=np.float32)
+    bits = torch.from_numpy(vals).to(torch.bfloat16)
+    assert torch.equal(bits.float(), torch.from_numpy(vals))  # every value is also a bf16
+    knew = bits.view(torch.int16).numpy().view(np.uint16).reshape(1, 1, -1)
+    kc = np.zeros((1, 1, 1, knew.shape[2]), np.uint8)
+    vc = np.zeros_like(kc)
+    assert oracle.write_kv_fp8(knew, knew, kc, vc, np.array([0]), scale, scale) == 0
+    assert np.array_equal(kc.reshape(-1), codes)
+    assert np.array_equal(oracle.dequant_e4m3(kc, scale).reshape(-1), vals.astype(np.float64))
