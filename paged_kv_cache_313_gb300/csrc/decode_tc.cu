@@ -53,6 +53,12 @@ namespace {
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 3
 #endif
+#ifndef PA_DECODE_FP8_STAGES
+#define PA_DECODE_FP8_STAGES 3
+#endif
+#ifndef PA_DECODE_FP8_CTAS_PER_SM
+#define PA_DECODE_FP8_CTAS_PER_SM 3
+#endif
 #ifndef PA_DECODE_CTAS_PER_SM
 #define PA_DECODE_CTAS_PER_SM 2
 #endif
@@ -74,7 +80,9 @@ struct TcCfg {
     static constexpr int kHalves = kRowBytes / 128;       // 128-byte segments (swizzle rows) of a token row
     static constexpr int kStageTok = 64;
     // bf16 D=128: 32 KiB stages; bf16 D=64 and e4m3 D=128: 16 KiB stages, so more of them fit
-    static constexpr int kStages = kHalves == 2 ? PA_DECODE_STAGES : kFp8 ? 5 : 2 * PA_DECODE_STAGES;
+    static constexpr int kStages = kHalves == 2 ? PA_DECODE_STAGES : kFp8 ? PA_DECODE_FP8_STAGES : 2 * PA_DECODE_STAGES;
+    // e4m3 pools: more, smaller CTAs per SM (more producers and consumers for the same bytes)
+    static constexpr int kCtasPerSm = kFp8 ? PA_DECODE_FP8_CTAS_PER_SM : PA_DECODE_CTAS_PER_SM;
     static constexpr int kConsumerWarps = 4;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kHalfBytes = kStageTok * 128;   // one half of a stage's K (or V) tile
@@ -88,12 +96,21 @@ struct TcCfg {
     static constexpr int kNew = kQ + kStages * kQBytes;
     static constexpr int kNewBytes = kFp8 ? 0 : 2 * D * 2;  // (no fused write into e4m3 pools)
     static constexpr int kCum = kNew + kStages * kNewBytes;  // int [kMaxSeqs + 1]
-    static constexpr int kInfo = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
+    // the consumers' cross-warp (m, l) exchange (two buffers of [warp][8] each), per-warp scan totals, item total
+    static constexpr int kRed = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
+    static constexpr int kRedBytes = 2 * 2 * kConsumerWarps * 8 * 4;
+    static constexpr int kScan = kRed + kRedBytes;
+    static constexpr int kInfo = kScan + 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
-    static constexpr int kEnd = kBars + 2 * kStages * 8;
+    static constexpr int kCtx = kBars + 2 * kStages * 8;
+    // an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA, and 1 KiB of each CTA's
+    // allocation goes to aligning the base; every array lives in the dynamic allocation
+    static constexpr int kSmemCap = 228 * 1024 / kCtasPerSm - 2 * 1024;
+    // the clamped context length of every sequence, where it fits (else read from global memory)
+    static constexpr int kCtxN = kCtx + kMaxSeqsPersistent * 4 <= kSmemCap ? kMaxSeqsPersistent : 0;
+    static constexpr int kEnd = kCtx + kCtxN * 4;
     static constexpr size_t kSmemBytes = 1024 + kEnd;
-    // an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA
-    static_assert((kSmemBytes + 1024) * PA_DECODE_CTAS_PER_SM <= 228 * 1024, "shared memory budget");
+    static_assert(kEnd <= kSmemCap, "shared memory budget");
 };
 
 // Byte offset, within a stage's K (or V) tile, of 128-byte row r of half 0,
@@ -129,7 +146,7 @@ __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int 
 }
 
 template <int D, bool kFp8>
-__global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_SM)
+__global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeParams p, int* work) {
     using C = TcCfg<D, kFp8>;
@@ -140,12 +157,16 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_S
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int* cum = reinterpret_cast<int*>(smem + C::kCum);
+    int* ctx = reinterpret_cast<int*>(smem + C::kCtx);  // clamped context lengths (when C::kCtxN > 0)
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + C::kInfo);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBars);
     uint64_t* empty = full + C::kStages;
-    __shared__ float red_m[2][C::kConsumerWarps][8], red_l[2][C::kConsumerWarps][8];
-    __shared__ int warp_tot[C::kThreads / 32];
-    __shared__ int s_total;
+    auto red_m = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed);
+    auto red_l = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed + C::kRedBytes / 2);
+    int* warp_tot = reinterpret_cast<int*>(smem + C::kScan);
+    int& s_total = warp_tot[C::kThreads / 32];
+    static_assert(C::kThreads / 32 + 1 <= 16, "scan totals");
+    auto context_of = [&](int s) { return C::kCtxN ? ctx[s] : decode_context(p, s, false); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
@@ -181,6 +202,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_S
         for (int i = 0; i < per && first + i < N; ++i) {
             cum[first + i] = run;
             const int L = decode_context(p, first + i, false);
+            if (C::kCtxN) ctx[first + i] = L;
             int pre;
             run += num_partitions(L - decode_start(p, first + i, L, &pre), p.partition) * Hkv;
         }
@@ -199,142 +221,190 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_S
 
     if (warp == C::kConsumerWarps) {
         // ================================================================ producer
+        // Per stage the producer only waits for its ring slot, publishes the
+        // stage's description and issues the copies: each item's block-table
+        // entries are loaded one item ahead, and the valid-token masks of a
+        // 32-block chunk of the table are worked out lane-parallel (lane l for
+        // the chunk's stage l) when the chunk is reached.
         if (lane == 0) {
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
         }
+        struct Item {
+            int s, split, kvh, nsplit, pre, j0, ntok, L;
+            bool grouped;
+        };
+        auto describe = [&](int it) {
+            Item d;
+            d.grouped = it < n_grouped;
+            if (d.grouped) {
+                // a cascade group's shared prefix for one kv head: tokens [0, P) of its first sequence,
+                // the group's G x members query rows at once (members * G <= 32)
+                const int g = it / Hkv;
+                d.kvh = it - g * Hkv;
+                int s0 = p.group_offsets[g];
+                int members = p.group_offsets[g + 1] - s0;
+                if (s0 < 0 || members < 1 || s0 + members > N || members * G > 32) {
+                    if (lane == 0) count_error(p.error_count);
+                    s0 = 0;
+                    members = 0;
+                }
+                int pre = 0;
+                if (members) decode_start(p, s0, context_of(s0), &pre);
+                d.s = s0;
+                d.nsplit = members;  // carried to the consumers in StageInfo::nsplit
+                d.split = pre;       // and the prefix length in StageInfo::split
+                d.pre = pre;
+                d.j0 = 0;
+                d.ntok = pre;
+                d.L = 0;
+            } else {
+                decode_item(cum, N, Hkv, it - n_grouped, d.s, d.split, d.kvh);
+                d.L = context_of(d.s);
+                const int j_first = decode_start(p, d.s, d.L, &d.pre);
+                d.nsplit = num_partitions(d.L - j_first, p.partition);
+                d.j0 = j_first + d.split * p.partition;
+                d.ntok = max(0, min(d.L, d.j0 + p.partition) - d.j0);
+            }
+            return d;
+        };
+        // raw table entry of block (chunk * 32 + lane) of an item; checked when the chunk is used
+        auto load_chunk = [&](const Item& d, int chunk) {
+            const int idx = chunk * 32 + lane;
+            return idx < (d.ntok + B - 1) / B ? p.block_tables[(size_t)d.s * p.max_blocks_per_seq + d.j0 / B + idx]
+                                              : -1;
+        };
+        const int bps = C::kStageTok / B;   // blocks per stage (B <= 64)
+        const int spc = 32 / bps;           // stages per 32-block chunk of the table
+        const uint32_t block_bytes = 2u * C::kHalves * B * 128u;  // K and V of one block and kv head
+
         int item = 0;
         if (lane == 0) item = atomicAdd(&work[0], 1);
         item = __shfl_sync(0xffffffffu, item, 0);
+        int nxt = 0;  // the item after this one, claimed one item ahead
+        if (lane == 0 && item < total) nxt = atomicAdd(&work[0], 1);
+        Item d{};
+        int raw = -1;
+        if (item < total) {
+            d = describe(item);
+            raw = load_chunk(d, 0);
+        }
         uint32_t stage_no = 0;  // stages issued by this CTA
         bool ok = true;
         while (item < total && ok) {
-            int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(&work[0], 1);  // fetch the next item early
-            int s, split, kvh, nsplit, pre, j0, ntok, L_item = 0;
-            const bool grouped = item < n_grouped;
-            if (grouped) {
-                // a cascade group's shared prefix for one kv head: tokens [0, P) of its first sequence,
-                // the group's G x members query rows at once (members * G <= 32)
-                const int g = item / Hkv;
-                kvh = item - g * Hkv;
-                s = p.group_offsets[g];
-                int members = p.group_offsets[g + 1] - s;
-                if (s < 0 || members < 1 || s + members > N || members * G > 32) {
-                    if (lane == 0) count_error(p.error_count);
-                    s = 0;
-                    members = 0;
-                }
-                const int L = members ? decode_context(p, s, false) : 0;
-                pre = 0;
-                if (members) decode_start(p, s, L, &pre);
-                nsplit = members;  // carried to the consumers in StageInfo::nsplit
-                split = pre;       // and the prefix length in StageInfo::split
-                j0 = 0;
-                ntok = pre;
-            } else {
-                decode_item(cum, N, Hkv, item - n_grouped, s, split, kvh);
-                const int L = decode_context(p, s, false);
-                L_item = L;
-                const int j_first = decode_start(p, s, L, &pre);
-                nsplit = num_partitions(L - j_first, p.partition);
-                j0 = j_first + split * p.partition;
-                ntok = max(0, min(L, j0 + p.partition) - j0);
-            }
-            const bool direct = !grouped && nsplit == 1 && pre == 0;
-            const int nst = max(1, (ntok + C::kStageTok - 1) / C::kStageTok);
-            const int nblk = (ntok + B - 1) / B;
-            const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq + j0 / B;
-            int chunk = -1, pb_lane = -1;
+            const int nst = max(1, (d.ntok + C::kStageTok - 1) / C::kStageTok);
+            const int nblk = (d.ntok + B - 1) / B;
+            int pb_lane = -1;                 // physical block of this lane's table entry in the current chunk
+            unsigned long long lvalid = 0ull; // lane l: valid-token mask of the chunk's stage l
+            int lnvb = 0;                     // and how many of its blocks are loaded
+            int item2 = total, raw2 = -1;
+            Item d2{};
             for (int st = 0; st < nst; ++st) {
                 const int slot = stage_no % C::kStages;
+                const int chunk = st / spc, l = st - chunk * spc;
+                if (l == 0) {
+                    if (chunk > 0) raw = load_chunk(d, chunk);
+                    pb_lane = -1;
+                    if (chunk * 32 + lane < nblk) {
+                        pb_lane = raw;
+                        if (raw < 0 || raw >= p.num_blocks) {
+                            count_error(p.error_count);
+                            pb_lane = -1;
+                        }
+                    }
+                    // lane l: stage chunk * spc + l
+                    const int t0l = (chunk * spc + lane) * C::kStageTok;
+                    const int ntl = max(0, min(C::kStageTok, d.ntok - t0l));
+                    lvalid = 0ull;
+                    lnvb = 0;
+                    for (int b = 0; b < bps; ++b) {
+                        const int pb = __shfl_sync(0xffffffffu, pb_lane, (lane * bps + b) & 31);
+                        const int cnt = min(B, ntl - b * B);
+                        if (pb >= 0 && cnt > 0) {
+                            lvalid |= (cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull)) << (b * B);
+                            ++lnvb;
+                        }
+                    }
+                    const int skip = d.grouped ? 0 : d.pre - (d.j0 + t0l);  // a tail's first stage: mask the prefix
+                    if (skip > 0) lvalid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
+                }
                 if (stage_no >= (uint32_t)C::kStages &&
                     !mbar_wait(&empty[slot], ((stage_no / C::kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 const int t0 = st * C::kStageTok;
-                const int nt = max(0, min(C::kStageTok, ntok - t0));
-                const int b0 = t0 / B;
-                const int nb = (nt + B - 1) / B;
-                if (nb > 0 && (b0 >> 5) != chunk) {  // a stage's blocks never straddle a 32-entry chunk
-                    chunk = b0 >> 5;
-                    const int idx = chunk * 32 + lane;
-                    pb_lane = -1;
-                    if (idx < nblk) {
-                        pb_lane = table[idx];
-                        if (pb_lane < 0 || pb_lane >= p.num_blocks) {
-                            count_error(p.error_count);
-                            pb_lane = -1;
-                        }
-                    }
-                }
-                unsigned long long valid = 0ull;
-                uint32_t bytes = st == 0 && !grouped ? (uint32_t)(G * D * 2) : 0u;
-                for (int b = 0; b < nb; ++b) {
-                    const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                    if (pb >= 0) {
-                        const int cnt = min(B, nt - b * B);
-                        const unsigned long long bits = cnt >= 64 ? ~0ull : ((1ull << cnt) - 1ull);
-                        valid |= bits << (b * B);
-                        bytes += 2u * C::kHalves * B * 128u;
-                    }
-                }
-                const int skip = grouped ? 0 : pre - (j0 + t0);  // a tail's first stage: mask the prefix tokens
-                if (skip > 0) valid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
+                const int nt = max(0, min(C::kStageTok, d.ntok - t0));
+                const int nbs = (nt + B - 1) / B;  // blocks of this stage
+                const int b0 = l * bps;            // its first block within the chunk
+                const unsigned long long valid = __shfl_sync(0xffffffffu, lvalid, l);
+                uint32_t bytes = (uint32_t)__shfl_sync(0xffffffffu, lnvb, l) * block_bytes;
+                if (st == 0 && !d.grouped) bytes += (uint32_t)(G * D * 2);
                 // pa_decode_write: the sequence's newest token (position L - 1) falls in this stage
                 int new_row = -1;
                 long long new_slot = -1;
-                if (p.k_new && !grouped) {
-                    const int jn = L_item - 1 - (j0 + t0);
-                    if (L_item > 0 && jn >= 0 && jn < nt) {
-                        const int pbn = __shfl_sync(0xffffffffu, pb_lane, (b0 + jn / B) & 31);
-                        if (pbn >= 0) {
-                            new_row = jn;
-                            new_slot = (long long)pbn * B + (L_item - 1) % B;
-                            bytes += (uint32_t)C::kNewBytes;
-                        }
+                if (C::kNewBytes && p.k_new && !d.grouped) {
+                    const int jn = d.L - 1 - (d.j0 + t0);
+                    const bool here = d.L > 0 && jn >= 0 && jn < nt;
+                    const int pbn = __shfl_sync(0xffffffffu, pb_lane, (b0 + (here ? jn / B : 0)) & 31);
+                    if (here && pbn >= 0) {
+                        new_row = jn;
+                        new_slot = (long long)pbn * B + (d.L - 1) % B;
+                        bytes += (uint32_t)C::kNewBytes;
                     }
                 }
                 if (lane == 0) {
                     StageInfo& inf = info[slot];
-                    inf.s = s;
-                    inf.kvh = kvh;
-                    inf.split = split;
-                    inf.nsplit = nsplit;
-                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) | (direct ? 4 : 0) | (grouped ? 16 : 0);
+                    inf.s = d.s;
+                    inf.kvh = d.kvh;
+                    inf.split = d.split;
+                    inf.nsplit = d.nsplit;
+                    inf.flags = (st == 0 ? 1 : 0) | (st == nst - 1 ? 2 : 0) |
+                                (!d.grouped && d.nsplit == 1 && d.pre == 0 ? 4 : 0) | (d.grouped ? 16 : 0);
                     inf.ntok = nt;
                     inf.valid = valid;
                     inf.new_row = new_row;
                     inf.new_slot = new_slot;
                     mbar_arrive_expect_tx(&full[slot], bytes);
                     if (new_row >= 0) {
-                        const size_t row = ((size_t)s * Hkv + kvh) * D;
+                        const size_t row = ((size_t)d.s * Hkv + d.kvh) * D;
                         bulk_load(smem + C::kNew + slot * C::kNewBytes,
                                   static_cast<const __nv_bfloat16*>(p.k_new) + row, (uint32_t)(D * 2), &full[slot]);
                         bulk_load(smem + C::kNew + slot * C::kNewBytes + D * 2,
                                   static_cast<const __nv_bfloat16*>(p.v_new) + row, (uint32_t)(D * 2), &full[slot]);
                     }
-                    if (st == 0 && !grouped)
+                    if (st == 0 && !d.grouped)
                         bulk_load(smem + C::kQ + slot * C::kQBytes,
                                   static_cast<const __nv_bfloat16*>(p.q) +
-                                      ((size_t)s * p.num_q_heads + (size_t)kvh * G) * D,
+                                      ((size_t)d.s * p.num_q_heads + (size_t)d.kvh * G) * D,
                                   (uint32_t)(G * D * 2), &full[slot]);
                 }
                 __syncwarp();  // the transaction count is armed before any copy is issued
-                // one lane per block issues that block's copies, so the stage's boxes go out together
+                // lanes [0, nbs) copy the stage's K blocks and lanes [nbs, 2 nbs) its V blocks, so the
+                // boxes go out together
                 uint8_t* kdst = smem + C::kRing + slot * C::kStageBytes;
-                uint8_t* vdst = kdst + C::kTileBytes;
-                const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
-                if (lane < nb && my_pb >= 0) {
-                    const int boff = lane * C::kHalves * B * 128;
-                    tma_load_3d(kdst + boff, &tmk, 0, my_pb * B, kvh * C::kHalves, &full[slot]);
-                    tma_load_3d(vdst + boff, &tmv, 0, my_pb * B, kvh * C::kHalves, &full[slot]);
-                }
+                const int isv = lane >= nbs;
+                const int b = lane - isv * nbs;
+                const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + (lane < 2 * nbs ? b : 0)) & 31);
+                if (lane < 2 * nbs && my_pb >= 0)
+                    tma_load_3d(kdst + isv * C::kTileBytes + b * C::kHalves * B * 128, isv ? &tmv : &tmk, 0,
+                                my_pb * B, d.kvh * C::kHalves, &full[slot]);
                 __syncwarp();
                 ++stage_no;
+                if (st == 0) {
+                    // the next item: its number (claimed one item ago), its description and its first
+                    // table chunk, loaded while this item streams; then claim the one after it
+                    item2 = __shfl_sync(0xffffffffu, nxt, 0);
+                    if (item2 < total) {
+                        d2 = describe(item2);
+                        raw2 = load_chunk(d2, 0);
+                        if (lane == 0) nxt = atomicAdd(&work[0], 1);
+                    }
+                }
             }
-            item = __shfl_sync(0xffffffffu, nxt, 0);
+            item = item2;
+            d = d2;
+            raw = raw2;
         }
         // terminator stage
         {
@@ -577,7 +647,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, PA_DECODE_CTAS_PER_S
                     if (mem >= inf.nsplit) continue;
                     const int sm = inf.s + mem;
                     int pre_m;
-                    decode_start(p, sm, decode_context(p, sm, false), &pre_m);
+                    decode_start(p, sm, context_of(sm), &pre_m);
                     const bool same = pre_m == inf.split;  // inf.split carries the group's prefix length
                     const size_t slot0 = decode_unit(p, sm, inf.kvh) * p.max_splits * G + head;
                     const float Ls = hsel ? L1 : L0;
@@ -697,9 +767,20 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
         return rc;
     if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8>), C::kSmemBytes)) != PA_OK)
         return rc;
-    // PA_DECODE_CTAS_PER_SM CTAs per SM, never more CTAs than the largest possible item count
+    // C::kCtasPerSm CTAs per SM (or as many as are resident at once, should fewer fit), never more
+    // CTAs than the largest possible item count: a persistent CTA that is not resident from the start finds
+    // the queue empty when it runs
+    static int resident = 0;
+    if (resident == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8>, C::kThreads,
+                                                          C::kSmemBytes) != cudaSuccess)
+            return check_launch();
+        if (n < 1) return PA_ERR_UNSUPPORTED;
+        resident = n < C::kCtasPerSm ? n : C::kCtasPerSm;
+    }
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
-    const long long slots = (long long)num_sms * PA_DECODE_CTAS_PER_SM;
+    const long long slots = (long long)num_sms * resident;
     int grid = (int)(max_items < slots ? max_items : slots);
     return launch_kernel(decode_tc_kernel<D, kFp8>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv,
                          p, p.work);
