@@ -1,5 +1,5 @@
-// decode_tc.cu — paged decode for bf16 pools on GB300: a persistent kernel
-// with TMA-staged K/V blocks and warp-level bf16 tensor-core MMAs.
+// decode_tc.cu — paged decode for bf16 and e4m3 pools on GB300: a persistent
+// kernel with TMA-staged K/V blocks and warp-level tensor-core MMAs.
 //
 // What it computes ("PagedAttention学习笔记", 三、算法流程与数据结构: the kernel
 // reads Q and the block table, gathers K/V block by block, then softmax(QK^T)V;
@@ -11,28 +11,37 @@
 // kv head); partitions are `partition` tokens (a multiple of 64).  Items are
 // numbered densely, sequence-major then partition then kv head, from a
 // prefix sum of the per-sequence item counts that every CTA computes once
-// from context_lens.  Two CTAs per SM take items from a global counter in
-// the workspace, so long and short sequences balance dynamically.  (Putting
-// every sequence's short last partition at the end of the queue was
-// measured 2% slower.)
+// from context_lens.  Persistent CTAs (two per SM for bf16 pools, three for
+// e4m3 pools) take items from a global counter in the workspace, so long and
+// short sequences balance dynamically.
 //
 // Inside a CTA:
-//  * Warp 4 is the producer.  It walks its items and, for each 64-token
-//    stage, resolves the stage's block-table entries (one coalesced warp load
-//    per 32 blocks) and issues one 3-D TMA copy per block of K and of V — a
-//    physical block of one kv head is B rows of head_dim contiguous bf16 at a
-//    row stride of Hkv*head_dim, one box {64 columns, B rows, D/64 halves}
-//    of the pool viewed as [128-byte segment][row][64] — plus, on an item's
-//    first stage, a 1-D bulk copy of the item's G query rows.  Boxes land
-//    128-byte swizzled (ldmatrix reads are bank-conflict free) in a ring of
-//    kStages stages, completion counted on mbarriers.  The producer streams straight across
-//    item boundaries, so there is no per-item start-up gap.
+//  * Warp 4 is the producer.  For each 64-token stage it waits for a free
+//    ring slot, publishes the stage's description (sequence, kv head,
+//    valid-token mask) and issues one 3-D TMA copy per block of K and of V —
+//    a physical block of one kv head is B rows of head_dim contiguous
+//    elements at a row stride of Hkv*head_dim, one box {128 bytes, B rows,
+//    row bytes/128 segments} of the pool viewed as [128-byte segment][row]
+//    [128 bytes] — from separate lanes, so the boxes go out together; on an
+//    item's first stage it adds a 1-D bulk copy of the item's G query rows.
+//    Everything else is off the per-stage path: the next item is claimed two
+//    stages before the current one's last and described (with its first 32
+//    block-table entries loaded, one per lane) a stage later, and the
+//    valid-token masks of the stages covering a 32-entry chunk of the table
+//    are worked out lane-parallel when the chunk is reached.  Claiming late
+//    keeps a CTA from holding more than the rest of one item when the queue
+//    runs dry.  Boxes land 128-byte swizzled (ldmatrix reads are bank-conflict
+//    free) in a ring of kStages stages, completion counted on mbarriers; the
+//    producer streams straight across item boundaries.
 //  * Warps 0-3 consume 16 tokens of each stage apiece.  The G <= 8 query
-//    heads form the N=8 side of m16n8k16 bf16 MMAs:
+//    heads form the N=8 side of m16n8k16 tensor-core MMAs:
 //        S^T[16 tok x 8 heads] = K[16 tok x D] . Q^T        (D/16 MMAs)
 //        O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T       (D/16 MMAs)
 //    P^T goes from the accumulator layout to the B-operand layout with one
 //    movmatrix transpose per 8x8 half.  Softmax is online, in base-2 units.
+//    bf16 pools use bf16 MMAs; e4m3 pools are widened to f16 in registers
+//    (two codes per conversion) and use f16 MMAs, with the queries, already
+//    scaled, in f16.
 //  * Tokens past the context or in blocks with an invalid table entry are
 //    masked (score -inf) and their V rows zeroed before the PV MMA, so stale
 //    or non-finite pool contents never reach the output.
@@ -52,6 +61,9 @@ namespace {
 // Ring depth and CTAs per SM (build-time knobs; the defaults are the measured best).
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 3
+#endif
+#ifndef PA_DECODE_CLAIM_STAGES
+#define PA_DECODE_CLAIM_STAGES 2
 #endif
 #ifndef PA_DECODE_FP8_STAGES
 #define PA_DECODE_FP8_STAGES 3
@@ -172,16 +184,18 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
     pdl_trigger();
     pdl_wait();
 
-    // ---- per-sequence item counts and their exclusive prefix sum (every CTA, once)
+    // ---- per-sequence item counts and their exclusive prefix sum (every CTA, once).  (Queueing
+    // every sequence's short last partition after all the whole ones was measured 5-7% slower.)
+    auto counted_items = [&](int L, int s) {
+        int pre;
+        return num_partitions(L - decode_start(p, s, L, &pre), p.partition) * Hkv;
+    };
     {
         const int per = (N + C::kThreads - 1) / C::kThreads;
         const int first = threadIdx.x * per;
         int local = 0;
-        for (int i = 0; i < per && first + i < N; ++i) {
-            const int L = decode_context(p, first + i, blockIdx.x == 0);
-            int pre;
-            local += num_partitions(L - decode_start(p, first + i, L, &pre), p.partition) * Hkv;
-        }
+        for (int i = 0; i < per && first + i < N; ++i)
+            local += counted_items(decode_context(p, first + i, blockIdx.x == 0), first + i);
         int incl = local;  // inclusive scan over the warp
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -203,8 +217,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
             cum[first + i] = run;
             const int L = decode_context(p, first + i, false);
             if (C::kCtxN) ctx[first + i] = L;
-            int pre;
-            run += num_partitions(L - decode_start(p, first + i, L, &pre), p.partition) * Hkv;
+            run += counted_items(L, first + i);
         }
         if (threadIdx.x == C::kThreads - 1) {
             int tot = 0;
@@ -217,7 +230,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
     // items: the cascade groups' shared prefixes (one per group and kv head) first, then the
     // (sequence, partition, kv head) items of the prefix sum
     const int n_grouped = p.group_offsets ? p.num_groups * Hkv : 0;
-    const int total = s_total + n_grouped;
+    const int total = n_grouped + s_total;
 
     if (warp == C::kConsumerWarps) {
         // ================================================================ producer
@@ -281,8 +294,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
         int item = 0;
         if (lane == 0) item = atomicAdd(&work[0], 1);
         item = __shfl_sync(0xffffffffu, item, 0);
-        int nxt = 0;  // the item after this one, claimed one item ahead
-        if (lane == 0 && item < total) nxt = atomicAdd(&work[0], 1);
+        int nxt = 0;  // the item after this one (lane 0), claimed a few stages before this one's last
         Item d{};
         int raw = -1;
         if (item < total) {
@@ -299,6 +311,10 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
             int lnvb = 0;                     // and how many of its blocks are loaded
             int item2 = total, raw2 = -1;
             Item d2{};
+            // The next item is claimed when PA_DECODE_CLAIM_STAGES stages of this one are left to issue and
+            // described (with its first table chunk loaded) one stage later, so the claim's latency is hidden
+            // while a CTA never holds more than the rest of one item when the queue runs dry.
+            const int claim_at = max(0, nst - PA_DECODE_CLAIM_STAGES), describe_at = min(nst - 1, claim_at + 1);
             for (int st = 0; st < nst; ++st) {
                 const int slot = stage_no % C::kStages;
                 const int chunk = st / spc, l = st - chunk * spc;
@@ -391,14 +407,12 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                                 my_pb * B, d.kvh * C::kHalves, &full[slot]);
                 __syncwarp();
                 ++stage_no;
-                if (st == 0) {
-                    // the next item: its number (claimed one item ago), its description and its first
-                    // table chunk, loaded while this item streams; then claim the one after it
+                if (st == claim_at && lane == 0) nxt = atomicAdd(&work[0], 1);
+                if (st == describe_at) {
                     item2 = __shfl_sync(0xffffffffu, nxt, 0);
                     if (item2 < total) {
                         d2 = describe(item2);
                         raw2 = load_chunk(d2, 0);
-                        if (lane == 0) nxt = atomicAdd(&work[0], 1);
                     }
                 }
             }
