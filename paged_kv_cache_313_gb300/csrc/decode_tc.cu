@@ -733,7 +733,8 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;
             const size_t slot_ws = unit * p.max_splits + inf.split + p.split_base;
             float* wo = p.ws_o + slot_ws * G * D;
-            for (int idx = tid; idx < G * D; idx += 32 * C::kConsumerWarps) {
+            // four consecutive columns per thread: one pass for G <= 4, two for G = 8
+            for (int idx = 4 * tid; idx < G * D; idx += 4 * 32 * C::kConsumerWarps) {
                 const int h = idx / D;
                 float M = -INFINITY;
 #pragma unroll
@@ -744,14 +745,24 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                     const float mw = red_m[par][w][h];
                     if (mw != -INFINITY) Ls += red_l[par][w][h] * fast_exp2(mw - M);
                 }
-                float acc = slabs[idx];
+                float4 acc = *reinterpret_cast<const float4*>(slabs + idx);
 #pragma unroll
-                for (int w = 1; w < C::kConsumerWarps; ++w) acc += slabs[w * 8 * D + idx];
-                const float val = Ls > 0.f ? acc / Ls * (kFp8 ? p.v_scale : 1.f) : 0.f;
+                for (int w = 1; w < C::kConsumerWarps; ++w) {
+                    const float4 v = *reinterpret_cast<const float4*>(slabs + w * 8 * D + idx);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                const float sc = Ls > 0.f ? (kFp8 ? p.v_scale : 1.f) / Ls : 0.f;
+                acc.x *= sc;
+                acc.y *= sc;
+                acc.z *= sc;
+                acc.w *= sc;
                 if (inf.flags & 4) {
-                    out[idx] = __float2bfloat16_rn(val);
+                    *reinterpret_cast<uint2*>(out + idx) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
                 } else {
-                    wo[idx] = val;
+                    *reinterpret_cast<float4*>(wo + idx) = acc;
                     if (idx % D == 0) p.ws_ml[slot_ws * G + h] = make_float2(M, Ls);
                 }
             }
@@ -858,7 +869,8 @@ bool decode_tc_supported(const DecodeParams& p, int dtype) {
     if (p.kv_fp8 && (p.head_dim != 128 || p.group_offsets || p.k_new)) return false;
     if (B != 8 && B != 16 && B != 32 && B != 64) return false;
     if (p.partition % 64 != 0 || p.num_seqs > kMaxSeqsPersistent) return false;
-    if (((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) || ((uintptr_t)p.q & 15)) return false;
+    if (((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) || ((uintptr_t)p.q & 15) || ((uintptr_t)p.out & 15))
+        return false;
     if ((long long)p.num_blocks * B >= (1LL << 31)) return false;
     return p.max_splits <= 128 && p.work != nullptr;
 }
