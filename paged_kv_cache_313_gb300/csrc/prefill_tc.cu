@@ -72,6 +72,22 @@ constexpr int kTmemSlot = kMask + kMaskSlots * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
+// The MMA-issuing thread waits by polling (it sits on the critical path of
+// every tile: a sleeping wait noticed the softmax's P about 750 cycles after
+// the last warp arrived); the softmax warps optionally too (build knobs).
+#ifndef PA_PREFILL_MMA_SPIN
+#define PA_PREFILL_MMA_SPIN 0
+#endif
+#ifndef PA_PREFILL_SOFTMAX_SPIN
+#define PA_PREFILL_SOFTMAX_SPIN 0
+#endif
+__device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity) {
+    return PA_PREFILL_MMA_SPIN ? mbar_wait_spin(bar, parity) : mbar_wait(bar, parity);
+}
+__device__ __forceinline__ bool softmax_wait(uint64_t* bar, uint32_t parity) {
+    return PA_PREFILL_SOFTMAX_SPIN ? mbar_wait_spin(bar, parity) : mbar_wait(bar, parity);
+}
+
 // the eight softmax warps (256 threads) only
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
@@ -179,11 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, r0 + i0, bars.q_full());
         }
         if (v_side && lane == 0 && nt > 0) tma_prefetch_desc(&tmv);
-        int chunk = -1, pb_lane = -1;
+        // Per key tile the producer only waits for its ring slot and issues the copies: the block ids of
+        // a 32-entry chunk of the table are loaded one per lane when the chunk is reached, and the
+        // tiles under that chunk get their key masks and byte counts lane-parallel (lane t for the
+        // chunk's tile t).
+        const int tpc = 32 / bpt;  // key tiles per 32-entry chunk of the table
+        int pb_lane = -1;
+        uint32_t lbytes = 0, lvm[4] = {0u, 0u, 0u, 0u};
         for (int j = 0; j < nt; ++j) {
-            const int b0 = j * bpt;
-            if ((b0 >> 5) != chunk) {  // a tile's blocks never straddle a 32-entry chunk
-                chunk = b0 >> 5;
+            const int chunk = j / tpc, l = j - chunk * tpc;
+            if (l == 0) {
                 const int idx = chunk * 32 + lane;
                 pb_lane = -1;
                 if (idx < nblk) {
@@ -193,26 +214,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pb_lane = -1;
                     }
                 }
-            }
-            uint32_t bytes = 0, vm[4] = {0u, 0u, 0u, 0u};
-            for (int b = 0; b < bpt; ++b) {
-                const int pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + b) & 31);
-                if (b0 + b < nblk && pb >= 0) {
-                    bytes += 2u * B * 128u;
-                    const int k0 = b * B, k1 = min((b + 1) * B, nkeys - j * kTileK);
+                const int jt = chunk * tpc + lane;  // this lane's key tile
+                lbytes = 0;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
-                        if (lo < hi) vm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                for (int w = 0; w < 4; ++w) lvm[w] = 0u;
+                for (int b = 0; b < bpt; ++b) {
+                    const int pb = __shfl_sync(0xffffffffu, pb_lane, (lane * bpt + b) & 31);
+                    if (lane < tpc && jt * bpt + b < nblk && pb >= 0) {
+                        lbytes += 2u * B * 128u;
+                        const int k0 = b * B, k1 = min((b + 1) * B, nkeys - jt * kTileK);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
+                            if (lo < hi) lvm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                        }
                     }
                 }
             }
-            const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + lane) & 31);
-            const bool my_load = lane < bpt && b0 + lane < nblk && my_pb >= 0;
+            const uint32_t bytes = __shfl_sync(0xffffffffu, lbytes, l);
+            // lanes [0, 2 bpt) copy the tile's blocks, one (block, 64-column half) box each
+            const int blk = lane >> 1, h = lane & 1;
+            const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (l * bpt + (lane < 2 * bpt ? blk : 0)) & 31);
+            const bool my_load = lane < 2 * bpt && j * bpt + blk < nblk && my_pb >= 0;
             if (!v_side) {
                 // K tile j (its slot is free once S_{j-3} completed; S_{j-3} was issued after PV_{j-5}, so
                 // the softmax warps have finished tile j-5 and read every mask up to j-5: the mask ring
                 // of 8 slots is never overwritten unread)
+                uint32_t vm[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) vm[w] = __shfl_sync(0xffffffffu, lvm[w], l);
                 const int st = j % kKStages;
                 if (j >= kKStages && !mbar_wait(bars.k_empty(st), ((j / kKStages) - 1) & 1)) ok = false;
                 if (!ok) break;
@@ -221,11 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(bars.m_full(j % kMaskSlots));
                     mbar_arrive_expect_tx(bars.k_full(st), bytes);
                 }
-                __syncwarp();  // armed before any copy is issued; then one lane per block issues its boxes
+                __syncwarp();  // armed before any copy is issued
                 if (my_load)
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + lane * B * 128, &tmk,
-                                    kvh * kD + h * 64, my_pb * B, bars.k_full(st));
+                    tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + blk * B * 128, &tmk, kvh * kD + h * 64,
+                                my_pb * B, bars.k_full(st));
             } else {
                 // V tile j (its slot is free once PV_{j-kVStages} completed)
                 const int vs = j % kVStages;
@@ -234,62 +263,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
                 __syncwarp();
                 if (my_load)
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + lane * B * 128, &tmv,
-                                    kvh * kD + h * 64, my_pb * B, bars.v_full(vs));
+                    tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + blk * B * 128, &tmv, kvh * kD + h * 64,
+                                my_pb * B, bars.v_full(vs));
             }
             __syncwarp();
         }
         if (!ok && lane == 0) count_error(p.error_count);
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
-            constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
-            const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
-            const uint32_t v_base = smem_u32(smem + kV);
-            const uint32_t t_oa = tmem + kTmemOa, t_ob = tmem + kTmemOb;
-            // descriptors of k-step 0; a k-step adds its byte offset >> 4 to the start-address field
-            const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
-            const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
-            const uint64_t dv0 = umma_desc_sw128(v_base, kHalf, 1024);
-            if (nt > 0 && !mbar_wait(bars.q_full(), 0)) ok = false;
-            for (int j = 0; j <= nt && ok; ++j) {
-                if (j < nt) {  // S_j = Q K_j^T into S[j%2]
-                    // S[j%2] last held P_{j-2}, read by PV_{j-2}, which was issued before this MMA (the
-                    // tensor core runs one thread's MMAs in order)
-                    const int st = j % kKStages, sb = j & 1;
-                    if (!mbar_wait(bars.k_full(st), (j / kKStages) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
+        // The whole warp runs the loop with warp-uniform descriptors; one elected lane issues every
+        // MMA and commit.  (Run by lane 0 alone, the same loop spent about 75 cycles per MMA issued.)
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mma_wait(bar, parity)) != 0;
+        };
+        constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
+        constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
+        const uint32_t q_base = smem_u32(smem + kQ), k_base = smem_u32(smem + kK);
+        const uint32_t v_base = smem_u32(smem + kV);
+        const uint32_t t_oa = tmem + kTmemOa, t_ob = tmem + kTmemOb;
+        // descriptors of k-step 0; a k-step adds its byte offset >> 4 to the start-address field
+        const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
+        const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
+        const uint64_t dv0 = umma_desc_sw128(v_base, kHalf, 1024);
+        if (nt > 0 && !wait_all(bars.q_full(), 0)) ok = false;
+        for (int j = 0; j <= nt && ok; ++j) {
+            if (j < nt) {  // S_j = Q K_j^T into S[j%2]
+                // S[j%2] last held P_{j-2}, read by PV_{j-2}, which was issued before this MMA (the
+                // tensor core runs one thread's MMAs in order)
+                const int st = j % kKStages, sb = j & 1;
+                if (!wait_all(bars.k_full(st), (j / kKStages) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                        umma_bf16(tmem + sb * 128, dq0 + off, dk + off, idesc_s, kk > 0);
-                    }
-                    umma_commit(bars.s_full(sb));
-                    umma_commit(bars.k_empty(st));
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                    umma_bf16_warp(tmem + sb * 128, dq0 + off, dk + off, idesc_s, kk > 0);
                 }
-                if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from tensor memory
-                    const int jj = j - 1, vs = jj % kVStages, pb = jj & 1;
-                    if (!mbar_wait(bars.p_full(pb), (jj >> 1) & 1)) { ok = false; break; }
-                    if (!mbar_wait(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < kTileK / 16; ++kk) {
-                        // keys 16kk..16kk+15: P columns 8kk.. (keys 0-63) or 64 + 8(kk-4).. (keys 64-127);
-                        // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
-                        const uint32_t pa = tmem + pb * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-                        umma_bf16_ta(kk < 4 ? t_oa : t_ob, pa, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                     jj > 0 || (kk & 3) > 0);
-                    }
-                    umma_commit(bars.o_done(pb));
-                    umma_commit(bars.v_empty(vs));
-                }
+                umma_commit_warp(bars.s_full(sb));
+                umma_commit_warp(bars.k_empty(st));
             }
-            if (!ok) count_error(p.error_count);
+            if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from tensor memory
+                const int jj = j - 1, vs = jj % kVStages, pb = jj & 1;
+                // V (usually landed long before) first, so that its poll is not on the path from P
+                if (!wait_all(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
+                if (!wait_all(bars.p_full(pb), (jj >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kTileK / 16; ++kk) {
+                    // keys 16kk..16kk+15: P columns 8kk.. (keys 0-63) or 64 + 8(kk-4).. (keys 64-127);
+                    // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
+                    const uint32_t pa = tmem + pb * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                    umma_bf16_ta_warp(kk < 4 ? t_oa : t_ob, pa, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                      jj > 0 || (kk & 3) > 0);
+                }
+                umma_commit_warp(bars.o_done(pb));
+                umma_commit_warp(bars.v_empty(vs));
+            }
         }
+        if (!ok && lane == 0) count_error(p.error_count);
         __syncwarp();
     } else {
         // ============================================================ softmax / epilogue
@@ -319,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t vm[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) vm[w] = vmask[(j % kMaskSlots) * 4 + w];
-            if (ok && !mbar_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
+            if (ok && !softmax_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
             tc_fence_after();
             float sv[64];
 #pragma unroll
@@ -335,19 +367,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dense: every key of my 64 is valid and causally visible, and the scale is positive,
             // so the max can be taken on raw scores and the scale folded into one FMA later
             const bool dense = (w0 & w1) == ~0u && kbase + 63 <= my_last && sl2 > 0.f;
-            float mpart = -INFINITY;
+            // row max over my 64 keys in eight independent chains (a single chain of 64 dependent
+            // maxima was a third of the softmax's time)
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
             if (dense) {
 #pragma unroll
-                for (int k = 0; k < 64; ++k) mpart = fmaxf(mpart, sv[k]);
-                mpart *= sl2;
+                for (int k = 0; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < 64; ++k) {
                     const bool valid = (((k < 32 ? w0 : w1) >> (k & 31)) & 1u) && kbase + k <= my_last;
                     sv[k] = valid ? sv[k] * sl2 : -INFINITY;
-                    mpart = fmaxf(mpart, sv[k]);
+                    mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
                 }
             }
+            float mpart = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            if (dense) mpart *= sl2;
             const float mt = mpart;
             if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
                 if (m_run != -INFINITY) {
@@ -386,11 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             {
                 uint32_t pk[32];
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    lsum += sv[2 * i] + sv[2 * i + 1];
+                    ls4[i & 3] += sv[2 * i] + sv[2 * i + 1];
                     pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
                 }
+                lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                 tmem_st32u(tmem + lane_off + st * 128 + col0, pk);
                 tmem_wait_st();
             }
