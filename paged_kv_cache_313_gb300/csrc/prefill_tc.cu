@@ -88,6 +88,12 @@ __device__ __forceinline__ bool softmax_wait(uint64_t* bar, uint32_t parity) {
     return PA_PREFILL_SOFTMAX_SPIN ? mbar_wait_spin(bar, parity) : mbar_wait(bar, parity);
 }
 
+// Dense tiles exponentiate in bf16 pairs (one instruction per two keys; P is
+// rounded to bf16 for its MMA either way, the pair form also rounds x - m).
+#ifndef PA_PREFILL_EXP2_PAIRS
+#define PA_PREFILL_EXP2_PAIRS 1
+#endif
+
 // the eight softmax warps (256 threads) only
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
             if (dense) {
 #pragma unroll
-                for (int k = 0; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+                for (int k = 0; k < 64; k += 2) mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], sv[k], sv[k + 1]);
             } else {
 #pragma unroll
                 for (int k = 0; k < 64; ++k) {
@@ -414,21 +420,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             // overwrites only S values it has already read)
             float lsum = 0.f;
             const float neg_m = -m_run;
-            if (dense) {
-#pragma unroll
-                for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
-            } else {
-#pragma unroll
-                for (int k = 0; k < 64; ++k)
-                    sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
-            }
             {
                 uint32_t pk[32];
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (PA_PREFILL_EXP2_PAIRS && dense) {
+                    // two keys per instruction throughout: x - m by a paired FMA, rounded to a bf16
+                    // pair, 2^x of the pair (which is P itself), and the sum of the same bf16 values
+                    // by a paired add
+                    const unsigned long long s2 = f32x2_pack(sl2, sl2), m2 = f32x2_pack(neg_m, neg_m);
+                    unsigned long long acc2[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    ls4[i & 3] += sv[2 * i] + sv[2 * i + 1];
-                    pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+                    for (int i = 0; i < 32; ++i) {
+                        float y0, y1;
+                        f32x2_unpack(fma_f32x2(f32x2_pack(sv[2 * i], sv[2 * i + 1]), s2, m2), y0, y1);
+                        const uint32_t e = exp2_bf16x2(pack_bf16x2(y0, y1));
+                        pk[i] = e;
+                        acc2[i & 1] = add_f32x2(
+                            acc2[i & 1], f32x2_pack(__uint_as_float(e << 16), __uint_as_float(e & 0xFFFF0000u)));
+                    }
+                    float a0, a1, b0, b1;
+                    f32x2_unpack(acc2[0], a0, a1);
+                    f32x2_unpack(acc2[1], b0, b1);
+                    ls4[0] = a0;
+                    ls4[1] = a1;
+                    ls4[2] = b0;
+                    ls4[3] = b1;
+                } else {
+                    if (dense) {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 64; ++k)
+                            sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        ls4[i & 3] += sv[2 * i] + sv[2 * i + 1];
+                        pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+                    }
                 }
                 lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                 tmem_st32u(tmem + lane_off + st * 128 + col0, pk);
@@ -448,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4*>(vrow + h * kHalf + r * 128 + c8 * 16) = z;
             }
-            fence_proxy_async_smem();
+            if (need_zero) fence_proxy_async_smem();  // the zeroed rows before the PV MMA reads them
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(bars.p_full(j & 1));
