@@ -69,6 +69,10 @@ namespace {
 #ifndef PA_DECODE_CLAIM_STAGES
 #define PA_DECODE_CLAIM_STAGES 2
 #endif
+// e4m3 pools with an even number of kv heads: items of two kv heads.
+#ifndef PA_DECODE_FP8_PAIRS
+#define PA_DECODE_FP8_PAIRS 1
+#endif
 #ifndef PA_DECODE_FP8_STAGES
 #define PA_DECODE_FP8_STAGES 3
 #endif
@@ -79,6 +83,7 @@ namespace {
 #define PA_DECODE_CTAS_PER_SM 2
 #endif
 constexpr int kMaxSeqsPersistent = PA_DECODE_CTAS_PER_SM == 1 ? 2048 : 1024;
+constexpr int kMaxSeqsPairs = 768;
 
 struct StageInfo {
     int s, kvh, split, nsplit;
@@ -90,21 +95,28 @@ struct StageInfo {
 };
 
 // kFp8: the pools hold e4m3 codes (one byte per element) instead of bf16.
-template <int D, bool kFp8>
+// kPair: an item covers two adjacent kv heads, whose rows sit next to each
+// other in the pool, so one box per block carries both (e4m3 pools: a 64-token
+// stage of two heads is as many bytes as one of a single bf16 head).
+template <int D, bool kFp8, bool kPair = false>
 struct TcCfg {
     static constexpr int kRowBytes = kFp8 ? D : 2 * D;   // one token row of one kv head
     static constexpr int kHalves = kRowBytes / 128;       // 128-byte segments (swizzle rows) of a token row
+    static constexpr int kHeads = kPair ? 2 : 1;          // kv heads per item
+    static constexpr int kSegs = kHalves * kHeads;        // segments per token row of a block's box
     static constexpr int kStageTok = 64;
     // bf16 D=128: 32 KiB stages; bf16 D=64 and e4m3 D=128: 16 KiB stages, so more of them fit
-    static constexpr int kStages = kHalves == 2 ? PA_DECODE_STAGES : kFp8 ? PA_DECODE_FP8_STAGES : 2 * PA_DECODE_STAGES;
-    // e4m3 pools: more, smaller CTAs per SM (more producers and consumers for the same bytes)
-    static constexpr int kCtasPerSm = kFp8 ? PA_DECODE_FP8_CTAS_PER_SM : PA_DECODE_CTAS_PER_SM;
+    static constexpr int kStages = kSegs == 2 ? PA_DECODE_STAGES : kFp8 ? PA_DECODE_FP8_STAGES : 2 * PA_DECODE_STAGES;
+    // e4m3 pools, one head per item: more, smaller CTAs per SM (more producers and consumers for the
+    // same bytes)
+    static constexpr int kCtasPerSm = kFp8 && !kPair ? PA_DECODE_FP8_CTAS_PER_SM : PA_DECODE_CTAS_PER_SM;
     static constexpr int kConsumerWarps = 4;
+    static constexpr int kWarpsPerHead = kConsumerWarps / kHeads;
     static constexpr int kThreads = (kConsumerWarps + 1) * 32;
     static constexpr int kHalfBytes = kStageTok * 128;   // one half of a stage's K (or V) tile
-    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kTileBytes = kSegs * kHalfBytes;
     static constexpr int kStageBytes = 2 * kTileBytes;   // K + V
-    static constexpr int kQBytes = 8 * D * 2;            // up to 8 query rows of the item
+    static constexpr int kQBytes = kHeads * 8 * D * 2;   // up to 8 query rows per kv head of the item
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kRing = 0;
     static constexpr int kQ = kRing + kStages * kStageBytes;
@@ -113,7 +125,10 @@ struct TcCfg {
     static constexpr int kNewBytes = kFp8 ? 0 : 2 * D * 2;  // (no fused write into e4m3 pools)
     static constexpr int kCum = kNew + kStages * kNewBytes;  // int [kMaxSeqs + 1]
     // the consumers' cross-warp (m, l) exchange (two buffers of [warp][8] each), per-warp scan totals, item total
-    static constexpr int kRed = kCum + ((kMaxSeqsPersistent + 1) * 4 + 63) / 64 * 64;
+    // sequences per launch (the prefix sum lives in shared memory; two-head items keep a shorter one so
+    // that their larger query slots fit)
+    static constexpr int kMaxSeqs = kPair ? kMaxSeqsPairs : kMaxSeqsPersistent;
+    static constexpr int kRed = kCum + ((kMaxSeqs + 1) * 4 + 63) / 64 * 64;
     static constexpr int kRedBytes = 2 * 2 * kConsumerWarps * 8 * 4;
     static constexpr int kScan = kRed + kRedBytes;
     static constexpr int kInfo = kScan + 64;
@@ -123,7 +138,7 @@ struct TcCfg {
     // allocation goes to aligning the base; every array lives in the dynamic allocation
     static constexpr int kSmemCap = 228 * 1024 / kCtasPerSm - 2 * 1024;
     // the clamped context length of every sequence, where it fits (else read from global memory)
-    static constexpr int kCtxN = kCtx + kMaxSeqsPersistent * 4 <= kSmemCap ? kMaxSeqsPersistent : 0;
+    static constexpr int kCtxN = kCtx + kMaxSeqs * 4 <= kSmemCap ? kMaxSeqs : 0;
     static constexpr int kEnd = kCtx + kCtxN * 4;
     static constexpr size_t kSmemBytes = 1024 + kEnd;
     static_assert(kEnd <= kSmemCap, "shared memory budget");
@@ -161,14 +176,16 @@ __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int 
     kvh = r - split * Hkv;
 }
 
-template <int D, bool kFp8>
-__global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCtasPerSm)
+template <int D, bool kFp8, bool kPair>
+__global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8, kPair>::kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeParams p, int* work) {
-    using C = TcCfg<D, kFp8>;
+    using C = TcCfg<D, kFp8, kPair>;
     static_assert(!kFp8 || D == 128, "fp8 pools: head_dim 128");
+    static_assert(!kPair || kFp8, "kv-head pairs: e4m3 pools");
     constexpr int KT = D / 16;  // 16-wide k steps (QK^T) and m tiles (PV)
     const int N = p.num_seqs, Hkv = p.num_kv_heads, G = p.group, B = p.block_size;
+    const int HkvI = Hkv / C::kHeads;  // items per partition
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -192,7 +209,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
     // every sequence's short last partition after all the whole ones was measured 5-7% slower.)
     auto counted_items = [&](int L, int s) {
         int pre;
-        return num_partitions(L - decode_start(p, s, L, &pre), p.partition) * Hkv;
+        return num_partitions(L - decode_start(p, s, L, &pre), p.partition) * HkvI;
     };
     {
         const int per = (N + C::kThreads - 1) / C::kThreads;
@@ -276,7 +293,8 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 d.ntok = pre;
                 d.L = 0;
             } else {
-                decode_item(cum, N, Hkv, it - n_grouped, d.s, d.split, d.kvh);
+                decode_item(cum, N, HkvI, it - n_grouped, d.s, d.split, d.kvh);
+                d.kvh *= C::kHeads;  // the item's first kv head
                 d.L = context_of(d.s);
                 const int j_first = decode_start(p, d.s, d.L, &d.pre);
                 d.nsplit = num_partitions(d.L - j_first, p.partition);
@@ -293,7 +311,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
         };
         const int bps = C::kStageTok / B;   // blocks per stage (B <= 64)
         const int spc = 32 / bps;           // stages per 32-block chunk of the table
-        const uint32_t block_bytes = 2u * C::kHalves * B * 128u;  // K and V of one block and kv head
+        const uint32_t block_bytes = 2u * C::kSegs * B * 128u;  // K and V of one block and the item's kv heads
 
         int item = 0;
         if (lane == 0) item = atomicAdd(&work[0], 1);
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 const int b0 = l * bps;            // its first block within the chunk
                 const unsigned long long valid = __shfl_sync(0xffffffffu, lvalid, l);
                 uint32_t bytes = (uint32_t)__shfl_sync(0xffffffffu, lnvb, l) * block_bytes;
-                if (st == 0 && !d.grouped) bytes += (uint32_t)(G * D * 2);
+                if (st == 0 && !d.grouped) bytes += (uint32_t)(C::kHeads * G * D * 2);
                 // pa_decode_write: the sequence's newest token (position L - 1) falls in this stage
                 int new_row = -1;
                 long long new_slot = -1;
@@ -397,7 +415,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                         bulk_load(smem + C::kQ + slot * C::kQBytes,
                                   static_cast<const __nv_bfloat16*>(p.q) +
                                       ((size_t)d.s * p.num_q_heads + (size_t)d.kvh * G) * D,
-                                  (uint32_t)(G * D * 2), &full[slot]);
+                                  (uint32_t)(C::kHeads * G * D * 2), &full[slot]);
                 }
                 __syncwarp();  // the transaction count is armed before any copy is issued
                 // lanes [0, nbs) copy the stage's K blocks and lanes [nbs, 2 nbs) its V blocks, so the
@@ -407,7 +425,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 const int b = lane - isv * nbs;
                 const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + (lane < 2 * nbs ? b : 0)) & 31);
                 if (lane < 2 * nbs && my_pb >= 0)
-                    tma_load_3d(kdst + isv * C::kTileBytes + b * C::kHalves * B * 128, isv ? &tmv : &tmk, 0,
+                    tma_load_3d(kdst + isv * C::kTileBytes + b * C::kSegs * B * 128, isv ? &tmv : &tmk, 0,
                                 my_pb * B, d.kvh * C::kHalves, &full[slot]);
                 __syncwarp();
                 ++stage_no;
@@ -439,7 +457,10 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
     } else {
         // ================================================================ consumers
         const int g4 = lane >> 2, c4 = lane & 3;
-        const int row0 = warp * 16;  // this warp's 16 token rows in every stage
+        // this warp's kv head within the item and its token rows in every stage: 16 rows of the one
+        // head, or 32 rows of one of the two
+        const int hp = C::kHeads == 2 ? warp >> 1 : 0;
+        const int row0 = C::kHeads == 2 ? (warp & 1) * 32 : warp * 16;
         const int tid = threadIdx.x;  // 0..127
         uint32_t qb[KT][2];
         float o[KT][4];
@@ -452,7 +473,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
         // base-2 score scale: fp8 pools fold the softmax scale into the f16 queries and the K scale here
         const float sl2 = kFp8 ? p.k_scale : p.scale_log2;
         int item_parity = 0;
-        const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kHalves * B * 128), __ffs(B) - 1};
+        const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kSegs * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
             const int slot = stage_no % C::kStages;
             if (!(PA_DECODE_SPIN & 2 ? mbar_wait_spin : mbar_wait)(&full[slot], (stage_no / C::kStages) & 1)) {
@@ -483,7 +504,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 for (int kk = 0; kk < KT; ++kk) {
                     const int base = (kk >> 1) * 32 + 4 * c4 + (kk & 1) * 2;
                     if (g4 < G) {
-                        const __nv_bfloat16* r = qs + g4 * D;
+                        const __nv_bfloat16* r = qs + (hp * G + g4) * D;
                         qb[kk][0] = pack_f16x2(__bfloat162float(r[base]) * qsc, __bfloat162float(r[base + 1]) * qsc);
                         qb[kk][1] = pack_f16x2(__bfloat162float(r[base + 16]) * qsc,
                                                __bfloat162float(r[base + 17]) * qsc);
@@ -521,7 +542,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                         for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<int4*>(vt + tr.row(r0c + r) + h * tr.half_stride +
+                                *reinterpret_cast<int4*>(vt + tr.row(r0c + r) + (hp * C::kHalves + h) * tr.half_stride +
                                                          ((lane & 1) * 4 + c) * 16) = z;
                     }
                     __syncwarp();
@@ -536,7 +557,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
 #pragma unroll
                     for (int kq = 0; kq < D / 32; ++kq) {
                         uint32_t raw[4], a[4];
-                        ldmatrix_x4(raw, kbase + tr.at(r, 0, 2 * kq + (lane >> 4)));
+                        ldmatrix_x4(raw, kbase + tr.at(r, hp, 2 * kq + (lane >> 4)));
 #pragma unroll
                         for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
                         mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
@@ -596,7 +617,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
 #pragma unroll
                     for (int kv = 0; kv < D / 32; ++kv) {
                         uint32_t raw[4], ev[4], od[4];
-                        ldmatrix_x4_trans(raw, vbase + tr.at(r, 0, 2 * kv + ((lane >> 3) & 1)));
+                        ldmatrix_x4_trans(raw, vbase + tr.at(r, hp, 2 * kv + ((lane >> 3) & 1)));
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
@@ -624,6 +645,13 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 // zeroes the invalid V rows of a chunk before it reads them; the writes are identical)
 #pragma unroll 1
                 for (int r0c = 0; r0c < inf.ntok; r0c += 16) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
+            } else if constexpr (C::kHeads == 2) {
+                // two chunks of 16 rows of this warp's head
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int r0c = row0 + 16 * c;
+                    if (r0c < inf.ntok) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
+                }
             } else if (row0 < inf.ntok) {
                 if (inf.new_row >= row0 && inf.new_row < row0 + 16) {
                     // pa_decode_write: the newest token's staged K and V rows go into this stage's tiles
@@ -708,9 +736,9 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 red_l[par][warp][2 * c4 + 1] = L1;
             }
             bar();  // every warp is done with this stage's K/V, and the states are visible
-            float M0 = -INFINITY, M1 = -INFINITY;
+            float M0 = -INFINITY, M1 = -INFINITY;  // over the warps that share this warp's kv head
 #pragma unroll
-            for (int w = 0; w < C::kConsumerWarps; ++w) {
+            for (int w = hp * C::kWarpsPerHead; w < (hp + 1) * C::kWarpsPerHead; ++w) {
                 M0 = fmaxf(M0, red_m[par][w][2 * c4]);
                 M1 = fmaxf(M1, red_m[par][w][2 * c4 + 1]);
             }
@@ -732,32 +760,34 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
             }
             fence_proxy_async_smem();  // these writes precede the slot's next TMA write
             bar();
-            const size_t unit = decode_unit(p, inf.s, inf.kvh);
+            // the item's query rows (G per kv head, the heads' rows adjacent in q and out)
             __nv_bfloat16* out =
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;
-            const size_t slot_ws = unit * p.max_splits + inf.split + p.split_base;
-            float* wo = p.ws_o + slot_ws * G * D;
-            // four consecutive columns per thread: one pass for G <= 4, two for G = 8
-            for (int idx = 4 * tid; idx < G * D; idx += 4 * 32 * C::kConsumerWarps) {
-                const int h = idx / D;
+            // four consecutive columns per thread: one pass for G <= 4 (one head), two for G = 8
+            for (int idx = 4 * tid; idx < C::kHeads * G * D; idx += 4 * 32 * C::kConsumerWarps) {
+                const int hr = idx / D, dc = idx - hr * D;
+                const int hh = C::kHeads == 2 ? hr / G : 0, h = hr - hh * G;  // kv head of the item, query row
+                const int w0 = hh * C::kWarpsPerHead;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[par][w][h]);
+                for (int w = 0; w < C::kWarpsPerHead; ++w) M = fmaxf(M, red_m[par][w0 + w][h]);
                 float Ls = 0.f;
 #pragma unroll
-                for (int w = 0; w < C::kConsumerWarps; ++w) {
-                    const float mw = red_m[par][w][h];
-                    if (mw != -INFINITY) Ls += red_l[par][w][h] * fast_exp2(mw - M);
+                for (int w = 0; w < C::kWarpsPerHead; ++w) {
+                    const float mw = red_m[par][w0 + w][h];
+                    if (mw != -INFINITY) Ls += red_l[par][w0 + w][h] * fast_exp2(mw - M);
                 }
-                float4 acc = *reinterpret_cast<const float4*>(slabs + idx);
+                float4 acc = *reinterpret_cast<const float4*>(slabs + (w0 * 8 + h) * D + dc);
 #pragma unroll
-                for (int w = 1; w < C::kConsumerWarps; ++w) {
-                    const float4 v = *reinterpret_cast<const float4*>(slabs + w * 8 * D + idx);
+                for (int w = 1; w < C::kWarpsPerHead; ++w) {
+                    const float4 v = *reinterpret_cast<const float4*>(slabs + ((w0 + w) * 8 + h) * D + dc);
                     acc.x += v.x;
                     acc.y += v.y;
                     acc.z += v.z;
                     acc.w += v.w;
                 }
+                const size_t slot_ws = decode_unit(p, inf.s, inf.kvh + hh) * p.max_splits + inf.split + p.split_base;
+                float* wo = p.ws_o + (slot_ws * G + h) * D + dc;
                 const float sc = Ls > 0.f ? (kFp8 ? p.v_scale : 1.f) / Ls : 0.f;
                 acc.x *= sc;
                 acc.y *= sc;
@@ -766,8 +796,8 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
                 if (inf.flags & 4) {
                     *reinterpret_cast<uint2*>(out + idx) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
                 } else {
-                    *reinterpret_cast<float4*>(wo + idx) = acc;
-                    if (idx % D == 0) p.ws_ml[slot_ws * G + h] = make_float2(M, Ls);
+                    *reinterpret_cast<float4*>(wo) = acc;
+                    if (dc == 0) p.ws_ml[slot_ws * G + h] = make_float2(M, Ls);
                 }
             }
             __syncwarp();
@@ -786,15 +816,17 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8>::kThreads, TcCfg<D, kFp8>::kCta
     }
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, bool kPair>
 int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-    using C = TcCfg<D, kFp8>;
+    using C = TcCfg<D, kFp8, kPair>;
     CUtensorMap tmk, tmv;
-    int rc = pool_tensor_map_rows(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8);
+    int rc = pool_tensor_map_rows(&tmk, p.k_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8, C::kHeads);
     if (rc != PA_OK) return rc;
-    if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8)) != PA_OK)
+    if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8,
+                                   C::kHeads)) != PA_OK)
         return rc;
-    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8>), C::kSmemBytes)) != PA_OK)
+    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8, kPair>), C::kSmemBytes)) !=
+        PA_OK)
         return rc;
     // C::kCtasPerSm CTAs per SM (or as many as are resident at once, should fewer fit), never more
     // CTAs than the largest possible item count: a persistent CTA that is not resident from the start finds
@@ -802,7 +834,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     static int resident = 0;
     if (resident == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8>, C::kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8, kPair>, C::kThreads,
                                                           C::kSmemBytes) != cudaSuccess)
             return check_launch();
         if (n < 1) return PA_ERR_UNSUPPORTED;
@@ -811,7 +843,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * resident;
     int grid = (int)(max_items < slots ? max_items : slots);
-    return launch_kernel(decode_tc_kernel<D, kFp8>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv,
+    return launch_kernel(decode_tc_kernel<D, kFp8, kPair>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv,
                          p, p.work);
 }
 
@@ -850,14 +882,14 @@ int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int bloc
 // (0, pb*B, kvh*D/64) is block pb's B rows of kv head kvh, stored
 // [segment][row][64] and 128-byte swizzled.
 int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                         int head_dim, bool fp8) {
+                         int head_dim, bool fp8, int heads_per_box) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
     // x: elements of one 128-byte segment; the segments of a row are 128 bytes apart
     const int esz = fp8 ? 1 : 2, seg = 128 / esz, row_bytes = num_kv_heads * head_dim * esz;
     cuuint64_t dims[3] = {(cuuint64_t)seg, (cuuint64_t)num_blocks * block_size, (cuuint64_t)row_bytes / 128};
     cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
-    cuuint32_t box[3] = {(cuuint32_t)seg, (cuuint32_t)block_size, (cuuint32_t)(head_dim * esz / 128)};
+    cuuint32_t box[3] = {(cuuint32_t)seg, (cuuint32_t)block_size, (cuuint32_t)(heads_per_box * head_dim * esz / 128)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void*>(pool), dims, strides, box, estr,
@@ -880,8 +912,12 @@ bool decode_tc_supported(const DecodeParams& p, int dtype) {
 }
 
 int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream) {
-    if (p.kv_fp8) return launch<128, true>(p, num_sms, stream);
-    return p.head_dim == 64 ? launch<64, false>(p, num_sms, stream) : launch<128, false>(p, num_sms, stream);
+    if (p.kv_fp8)
+        return PA_DECODE_FP8_PAIRS && p.num_kv_heads % 2 == 0 && p.num_seqs <= kMaxSeqsPairs
+                   ? launch<128, true, true>(p, num_sms, stream)
+                                                             : launch<128, true, false>(p, num_sms, stream);
+    return p.head_dim == 64 ? launch<64, false, false>(p, num_sms, stream)
+                            : launch<128, false, false>(p, num_sms, stream);
 }
 
 }  // namespace pa

@@ -22,7 +22,7 @@ int pool_tensor_map(CUtensorMap* map, const void* pool, int num_blocks, int bloc
 // every 128-byte segment of the row ([segment][row][128 bytes] in shared
 // memory): {64, B, D/64} for bf16, {128, B, D/128} for e4m3 pools.
 int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int num_kv_heads,
-                         int head_dim, bool fp8 = false);
+                         int head_dim, bool fp8 = false, int heads_per_box = 1);
 
 constexpr uint32_t kSpinLimit = 1u << 18;
 

@@ -527,13 +527,15 @@ def test_fp8_write_of_every_bf16_value_matches_oracle(k_scale, v_scale):
 
 FP8_DECODE_CASES = [
     # (Hq, Hkv, B, decode context lengths, code range): every block size, groups 1..8, partition boundaries,
-    # and codes over the whole finite range (subnormals up to 448) through the in-register conversion
+    # and codes over the whole finite range (subnormals up to 448) through the in-register conversion; even
+    # kv-head counts run items of two kv heads
     (8, 8, 8, [1, 63, 64, 65, 700], (0x30, 0x60)),
     (16, 8, 16, [5, 512, 513, 2000], (0x30, 0x60)),
     (32, 8, 32, [3000, 17, 129], (0x30, 0x60)),
     (64, 8, 64, [1, 100, 4097], (0x30, 0x60)),
     (32, 8, 16, [900, 64, 1], (0x00, 0x7F)),
     (16, 2, 8, [1025, 64], (0x00, 0x7F)),
+    (12, 3, 16, [700, 33, 1, 1200], (0x30, 0x60)),  # odd kv-head count: one kv head per item
 ]
 
 
