@@ -7,9 +7,13 @@
 // p = q_start_pos[c] + i, attends keys 0..p of its sequence, the chunk's own
 // keys included (they were written to the pool first).
 //
-// One CTA per (128-row query tile, kv head, chunk).  The G query heads that
-// share a kv head are packed into the tile's rows: row r is position
-// i0 + r/G, head r%G, so every K/V tile is loaded once for all G heads.
+// A work item is a (128-row query tile, kv head, chunk).  The G query heads
+// that share a kv head are packed into the tile's rows: row r is position
+// i0 + r/G, head r%G, so every K/V tile is loaded once for all G heads.  The
+// kernel is persistent: one CTA per SM walks its share of the items (the
+// heaviest tile of every chunk first), its K/V rings, barriers and tensor
+// memory carrying on from item to item, so one item's epilogue overlaps the
+// next item's loads and a CTA is set up once.
 // Key tiles are 128 keys, gathered block by block from the pool by TMA
 // (one box per physical block and 64-column half, 128-byte swizzled).
 //
@@ -65,8 +69,9 @@ constexpr int kQ = 0;
 constexpr int kK = kQ + kTileBytes;
 constexpr int kV = kK + kKStages * kTileBytes;
 constexpr int kBars = kV + kVStages * kTileBytes;
-// barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2], o_done[2], m_full[8]
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + kMaskSlots;
+// barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2], o_done[2], m_full[8],
+// q_empty, o_free
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + kMaskSlots + 2;
 constexpr int kMask = kBars + kNumBars * 8;  // uint32 [8][4]: key-validity mask of tile j in slot j%8
 constexpr int kTmemSlot = kMask + kMaskSlots * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
@@ -111,6 +116,10 @@ struct Bars {
     __device__ uint64_t* o_done(int i) const { return base + 5 + 2 * kKStages + 2 * kVStages + i; }
     // mask slot i published
     __device__ uint64_t* m_full(int i) const { return base + 7 + 2 * kKStages + 2 * kVStages + i; }
+    // the Q buffer may be refilled: every QK^T of the item has completed
+    __device__ uint64_t* q_empty() const { return base + 7 + 2 * kKStages + 2 * kVStages + kMaskSlots; }
+    // the softmax warps have read O (and left the S buffers) in an item's epilogue
+    __device__ uint64_t* o_free() const { return base + 8 + 2 * kKStages + 2 * kVStages + kMaskSlots; }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -118,37 +127,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
     pdl_trigger();
     pdl_wait();
-    const int c = blockIdx.z, kvh = blockIdx.y;
     const int G = p.group, B = p.block_size;
     const int pos_per_tile = kTileQ / G;
-
-    // ---- chunk descriptor (every thread, identical)
     const bool prefix_mode = p.prefix_lens != nullptr;
-    const int r0 = p.cu_q_lens[c];
-    const int n = p.cu_q_lens[c + 1] - r0;
-    const int s = prefix_mode ? r0 : p.seq_of_chunk[c];
-    int start = prefix_mode ? 0 : p.q_start_pos[c];
-    bool chunk_ok = n >= 0 && r0 >= 0 && r0 + n <= p.total_q && n <= p.max_q_len && s >= 0 && s < p.num_seqs;
-    if (chunk_ok && prefix_mode && n > 0) start = p.prefix_lens[s];  // the group's shared prefix length
-    chunk_ok = chunk_ok && start >= 0;
-    if (!chunk_ok) {
-        if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0) count_error(p.error_count);
-        return;
-    }
-    const int ntiles_q = (n + pos_per_tile - 1) / pos_per_tile;
-    if ((int)blockIdx.x >= ntiles_q) return;
-    const int tile = ntiles_q - 1 - blockIdx.x;  // heaviest (latest) tiles first
-    const int i0 = tile * pos_per_tile;
-    const int nq = min(pos_per_tile, n - i0);
-    const int cap = min(p.context_lens[s], p.max_blocks_per_seq * B);
-    // the tile's last query position; a cascade prefix pass reads keys [0, start) for every row
-    int last_key = prefix_mode ? start - 1 : start + i0 + nq - 1;
-    if (last_key >= cap) {
-        if (threadIdx.x == 0) count_error(p.error_count);
-        last_key = cap - 1;
-    }
-    const int nkeys = last_key + 1;  // keys 0..last_key are read
-    const int nt = nkeys > 0 ? (nkeys + kTileK - 1) / kTileK : 0;
+
+    // ---- work items: (query tile, kv head, chunk), the heaviest (latest) tile of every chunk first,
+    // then the next heaviest, ...; CTA b takes items b, b + grid, b + 2 grid, ...  Every warp walks the
+    // same items, so the roles agree without communicating.
+    const int tiles_max = (p.max_q_len + pos_per_tile - 1) / pos_per_tile;
+    const int per_rank = p.num_chunks * p.num_kv_heads;
+    const int num_items = tiles_max * per_rank;
+    struct Item {
+        int kvh, r0, s, start, i0, nq, last_key, nkeys, nt;
+    };
+    // false for an empty item (a tile past its chunk's queries, or an invalid chunk)
+    auto describe = [&](int k, Item& d) {
+        const int rank = k / per_rank, rem = k - rank * per_rank;
+        const int c = rem / p.num_kv_heads;
+        d.kvh = rem - c * p.num_kv_heads;
+        d.r0 = p.cu_q_lens[c];
+        const int n = p.cu_q_lens[c + 1] - d.r0;
+        d.s = prefix_mode ? d.r0 : p.seq_of_chunk[c];
+        d.start = prefix_mode ? 0 : p.q_start_pos[c];
+        bool chunk_ok =
+            n >= 0 && d.r0 >= 0 && d.r0 + n <= p.total_q && n <= p.max_q_len && d.s >= 0 && d.s < p.num_seqs;
+        if (chunk_ok && prefix_mode && n > 0) d.start = p.prefix_lens[d.s];  // the group's shared prefix length
+        chunk_ok = chunk_ok && d.start >= 0;
+        if (!chunk_ok) {
+            if (rank == 0 && d.kvh == 0 && threadIdx.x == 0) count_error(p.error_count);
+            return false;
+        }
+        const int ntiles_q = (n + pos_per_tile - 1) / pos_per_tile;
+        if (rank >= ntiles_q) return false;
+        d.i0 = (ntiles_q - 1 - rank) * pos_per_tile;
+        d.nq = min(pos_per_tile, n - d.i0);
+        const int cap = min(p.context_lens[d.s], p.max_blocks_per_seq * B);
+        // the tile's last query position; a cascade prefix pass reads keys [0, start) for every row
+        d.last_key = prefix_mode ? d.start - 1 : d.start + d.i0 + d.nq - 1;
+        if (d.last_key >= cap) {
+            if (threadIdx.x == 0) count_error(p.error_count);
+            d.last_key = cap - 1;
+        }
+        d.nkeys = d.last_key + 1;  // keys 0..last_key are read
+        d.nt = d.nkeys > 0 ? (d.nkeys + kTileK - 1) / kTileK : 0;
+        return true;
+    };
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars.o_done(i), 1);
         }
         for (int i = 0; i < kMaskSlots; ++i) mbar_init(bars.m_full(i), 1);
+        mbar_init(bars.q_empty(), 1);
+        mbar_init(bars.o_free(), 8);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -190,89 +215,110 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp 0 loads Q, the K tiles and publishes each tile's key mask; warp kVWarp loads the V
         // tiles.  Each waits only on its own ring, so K streams ahead of V.
         const bool v_side = warp == kVWarp;
-        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-        const int nblk = (nkeys + B - 1) / B;
         const int bpt = kTileK / B;  // blocks per key tile
-        if (!v_side && lane == 0 && nt > 0) {  // with no keys nothing is loaded (nor left in flight)
-            tma_prefetch_desc(&tmq);
-            tma_prefetch_desc(&tmk);
-            mbar_arrive_expect_tx(bars.q_full(), 2 * kHalf);
-            for (int h = 0; h < 2; ++h)
-                tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, r0 + i0, bars.q_full());
-        }
-        if (v_side && lane == 0 && nt > 0) tma_prefetch_desc(&tmv);
         // Per key tile the producer only waits for its ring slot and issues the copies: the block ids of
         // a 32-entry chunk of the table are loaded one per lane when the chunk is reached, and the
         // tiles under that chunk get their key masks and byte counts lane-parallel (lane t for the
-        // chunk's tile t).
+        // chunk's tile t).  The rings run on across items.
         const int tpc = 32 / bpt;  // key tiles per 32-entry chunk of the table
-        int pb_lane = -1;
-        uint32_t lbytes = 0, lvm[4] = {0u, 0u, 0u, 0u};
-        for (int j = 0; j < nt; ++j) {
-            const int chunk = j / tpc, l = j - chunk * tpc;
-            if (l == 0) {
-                const int idx = chunk * 32 + lane;
-                pb_lane = -1;
-                if (idx < nblk) {
-                    pb_lane = table[idx];
-                    if (pb_lane < 0 || pb_lane >= p.num_blocks) {
-                        if (!v_side) count_error(p.error_count);
-                        pb_lane = -1;
-                    }
+        if (lane == 0) {
+            if (!v_side) {
+                tma_prefetch_desc(&tmq);
+                tma_prefetch_desc(&tmk);
+            } else {
+                tma_prefetch_desc(&tmv);
+            }
+        }
+        int gt = 0, gi = 0;  // key tiles, and items with keys, taken so far
+        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x) {
+            Item d;
+            if (!describe(k, d)) continue;
+            const int kvh = d.kvh, nkeys = d.nkeys, nt = d.nt;
+            const int32_t* table = p.block_tables + (size_t)d.s * p.max_blocks_per_seq;
+            const int nblk = (nkeys + B - 1) / B;
+            if (!v_side && nt > 0) {  // with no keys nothing is loaded (nor left in flight)
+                // the Q tile; its buffer is free once the previous item's last QK^T completed
+                if (gi > 0 && !mbar_wait(bars.q_empty(), (gi - 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                const int jt = chunk * tpc + lane;  // this lane's key tile
-                lbytes = 0;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bars.q_full(), 2 * kHalf);
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, d.r0 + d.i0, bars.q_full());
+                }
+            }
+            int pb_lane = -1;
+            uint32_t lbytes = 0, lvm[4] = {0u, 0u, 0u, 0u};
+            for (int j = 0; j < nt; ++j) {
+                const int g = gt + j;  // the CTA's key tile number: ring slots and phases
+                const int chunk = j / tpc, l = j - chunk * tpc;
+                if (l == 0) {
+                    const int idx = chunk * 32 + lane;
+                    pb_lane = -1;
+                    if (idx < nblk) {
+                        pb_lane = table[idx];
+                        if (pb_lane < 0 || pb_lane >= p.num_blocks) {
+                            if (!v_side) count_error(p.error_count);
+                            pb_lane = -1;
+                        }
+                    }
+                    const int jt = chunk * tpc + lane;  // this lane's key tile
+                    lbytes = 0;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) lvm[w] = 0u;
-                for (int b = 0; b < bpt; ++b) {
-                    const int pb = __shfl_sync(0xffffffffu, pb_lane, (lane * bpt + b) & 31);
-                    if (lane < tpc && jt * bpt + b < nblk && pb >= 0) {
-                        lbytes += 2u * B * 128u;
-                        const int k0 = b * B, k1 = min((b + 1) * B, nkeys - jt * kTileK);
+                    for (int w = 0; w < 4; ++w) lvm[w] = 0u;
+                    for (int b = 0; b < bpt; ++b) {
+                        const int pb = __shfl_sync(0xffffffffu, pb_lane, (lane * bpt + b) & 31);
+                        if (lane < tpc && jt * bpt + b < nblk && pb >= 0) {
+                            lbytes += 2u * B * 128u;
+                            const int k0 = b * B, k1 = min((b + 1) * B, nkeys - jt * kTileK);
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
-                            if (lo < hi) lvm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                            for (int w = 0; w < 4; ++w) {
+                                const int lo = max(k0, 32 * w), hi = min(k1, 32 * w + 32);
+                                if (lo < hi) lvm[w] |= (hi - lo == 32 ? ~0u : ((1u << (hi - lo)) - 1u)) << (lo - 32 * w);
+                            }
                         }
                     }
                 }
-            }
-            const uint32_t bytes = __shfl_sync(0xffffffffu, lbytes, l);
-            // lanes [0, 2 bpt) copy the tile's blocks, one (block, 64-column half) box each
-            const int blk = lane >> 1, h = lane & 1;
-            const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (l * bpt + (lane < 2 * bpt ? blk : 0)) & 31);
-            const bool my_load = lane < 2 * bpt && j * bpt + blk < nblk && my_pb >= 0;
-            if (!v_side) {
-                // K tile j (its slot is free once S_{j-3} completed; S_{j-3} was issued after PV_{j-5}, so
-                // the softmax warps have finished tile j-5 and read every mask up to j-5: the mask ring
-                // of 8 slots is never overwritten unread)
-                uint32_t vm[4];
+                const uint32_t bytes = __shfl_sync(0xffffffffu, lbytes, l);
+                // lanes [0, 2 bpt) copy the tile's blocks, one (block, 64-column half) box each
+                const int blk = lane >> 1, h = lane & 1;
+                const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (l * bpt + (lane < 2 * bpt ? blk : 0)) & 31);
+                const bool my_load = lane < 2 * bpt && j * bpt + blk < nblk && my_pb >= 0;
+                if (!v_side) {
+                    // K tile j (its slot is free once S_{j-3} completed; S_{j-3} was issued after PV_{j-5}, so
+                    // the softmax warps have finished tile j-5 and read every mask up to j-5: the mask ring
+                    // of 8 slots is never overwritten unread)
+                    uint32_t vm[4];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) vm[w] = __shfl_sync(0xffffffffu, lvm[w], l);
-                const int st = j % kKStages;
-                if (j >= kKStages && !mbar_wait(bars.k_empty(st), ((j / kKStages) - 1) & 1)) ok = false;
-                if (!ok) break;
-                if (lane == 0) {
-                    for (int w = 0; w < 4; ++w) vmask[(j % kMaskSlots) * 4 + w] = vm[w];
-                    mbar_arrive(bars.m_full(j % kMaskSlots));
-                    mbar_arrive_expect_tx(bars.k_full(st), bytes);
+                    for (int w = 0; w < 4; ++w) vm[w] = __shfl_sync(0xffffffffu, lvm[w], l);
+                    const int st = g % kKStages;
+                    if (g >= kKStages && !mbar_wait(bars.k_empty(st), ((g / kKStages) - 1) & 1)) ok = false;
+                    if (!ok) break;
+                    if (lane == 0) {
+                        for (int w = 0; w < 4; ++w) vmask[(g % kMaskSlots) * 4 + w] = vm[w];
+                        mbar_arrive(bars.m_full(g % kMaskSlots));
+                        mbar_arrive_expect_tx(bars.k_full(st), bytes);
+                    }
+                    __syncwarp();  // armed before any copy is issued
+                    if (my_load)
+                        tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + blk * B * 128, &tmk, kvh * kD + h * 64,
+                                    my_pb * B, bars.k_full(st));
+                } else {
+                    // V tile j (its slot is free once PV_{j-kVStages} completed)
+                    const int vs = g % kVStages;
+                    if (g >= kVStages && !mbar_wait(bars.v_empty(vs), ((g / kVStages) - 1) & 1)) ok = false;
+                    if (!ok) break;
+                    if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
+                    __syncwarp();
+                    if (my_load)
+                        tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + blk * B * 128, &tmv, kvh * kD + h * 64,
+                                    my_pb * B, bars.v_full(vs));
                 }
-                __syncwarp();  // armed before any copy is issued
-                if (my_load)
-                    tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + blk * B * 128, &tmk, kvh * kD + h * 64,
-                                my_pb * B, bars.k_full(st));
-            } else {
-                // V tile j (its slot is free once PV_{j-kVStages} completed)
-                const int vs = j % kVStages;
-                if (j >= kVStages && !mbar_wait(bars.v_empty(vs), ((j / kVStages) - 1) & 1)) ok = false;
-                if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
                 __syncwarp();
-                if (my_load)
-                    tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + blk * B * 128, &tmv, kvh * kD + h * 64,
-                                my_pb * B, bars.v_full(vs));
             }
-            __syncwarp();
+            gt += nt;
+            if (nt > 0) ++gi;
         }
         if (!ok && lane == 0) count_error(p.error_count);
     } else if (warp == 1) {
@@ -291,41 +337,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dq0 = umma_desc_sw128(q_base, 16, 1024);
         const uint64_t dk0 = umma_desc_sw128(k_base, 16, 1024);
         const uint64_t dv0 = umma_desc_sw128(v_base, kHalf, 1024);
-        if (nt > 0 && !wait_all(bars.q_full(), 0)) ok = false;
-        for (int j = 0; j <= nt && ok; ++j) {
-            if (j < nt) {  // S_j = Q K_j^T into S[j%2]
-                // S[j%2] last held P_{j-2}, read by PV_{j-2}, which was issued before this MMA (the
-                // tensor core runs one thread's MMAs in order)
-                const int st = j % kKStages, sb = j & 1;
-                if (!wait_all(bars.k_full(st), (j / kKStages) & 1)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-                    umma_bf16_warp(tmem + sb * 128, dq0 + off, dk + off, idesc_s, kk > 0);
-                }
-                umma_commit_warp(bars.s_full(sb));
-                umma_commit_warp(bars.k_empty(st));
+        int gt = 0, gi = 0;  // key tiles, and items with keys, taken so far
+        for (int k = blockIdx.x; k < num_items && ok; k += gridDim.x) {
+            Item d;
+            if (!describe(k, d) || d.nt == 0) continue;
+            const int nt = d.nt;
+            if (!wait_all(bars.q_full(), gi & 1)) {
+                ok = false;
+                break;
             }
-            if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from tensor memory
-                const int jj = j - 1, vs = jj % kVStages, pb = jj & 1;
-                // V (usually landed long before) first, so that its poll is not on the path from P
-                if (!wait_all(bars.v_full(vs), (jj / kVStages) & 1)) { ok = false; break; }
-                if (!wait_all(bars.p_full(pb), (jj >> 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < kTileK / 16; ++kk) {
-                    // keys 16kk..16kk+15: P columns 8kk.. (keys 0-63) or 64 + 8(kk-4).. (keys 64-127);
-                    // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
-                    const uint32_t pa = tmem + pb * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-                    umma_bf16_ta_warp(kk < 4 ? t_oa : t_ob, pa, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                                      jj > 0 || (kk & 3) > 0);
-                }
-                umma_commit_warp(bars.o_done(pb));
-                umma_commit_warp(bars.v_empty(vs));
+            // the previous item's epilogue has read O and left the S buffers
+            if (gi > 0 && !wait_all(bars.o_free(), (gi - 1) & 1)) {
+                ok = false;
+                break;
             }
+            for (int j = 0; j <= nt && ok; ++j) {
+                if (j < nt) {  // S_j = Q K_j^T into S[g%2]
+                    // S[g%2] last held P_{g-2}, read by PV_{g-2}, which was issued before this MMA (the
+                    // tensor core runs one thread's MMAs in order)
+                    const int g = gt + j, st = g % kKStages, sb = g & 1;
+                    if (!wait_all(bars.k_full(st), (g / kKStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dk = dk0 + (uint64_t)((st * kTileBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t off = (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+                        umma_bf16_warp(tmem + sb * 128, dq0 + off, dk + off, idesc_s, kk > 0);
+                    }
+                    umma_commit_warp(bars.s_full(sb));
+                    umma_commit_warp(bars.k_empty(st));
+                    if (j == nt - 1) umma_commit_warp(bars.q_empty());  // every QK^T of the item is done with Q
+                }
+                if (j >= 1) {  // O += P_{j-1} V_{j-1}, P from tensor memory
+                    const int jj = j - 1, g = gt + jj, vs = g % kVStages, pb = g & 1;
+                    // V (usually landed long before) first, so that its poll is not on the path from P
+                    if (!wait_all(bars.v_full(vs), (g / kVStages) & 1)) { ok = false; break; }
+                    if (!wait_all(bars.p_full(pb), (g >> 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dv = dv0 + (uint64_t)((vs * kTileBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        // keys 16kk..16kk+15: P columns 8kk.. (keys 0-63) or 64 + 8(kk-4).. (keys 64-127);
+                        // keys 0-63 into O_a, keys 64-127 into O_b: each half of the row keeps its own max
+                        const uint32_t pa = tmem + pb * 128 + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+                        umma_bf16_ta_warp(kk < 4 ? t_oa : t_ob, pa, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                                          jj > 0 || (kk & 3) > 0);
+                    }
+                    umma_commit_warp(bars.o_done(pb));
+                    umma_commit_warp(bars.v_empty(vs));
+                }
+            }
+            gt += nt;
+            ++gi;
         }
         if (!ok && lane == 0) count_error(p.error_count);
         __syncwarp();
@@ -344,213 +407,232 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const int col0 = half * 64;
         const uint32_t t_own = tmem + lane_off + (half ? kTmemOb : kTmemOa);  // this half's O, row r
-        const int pos = i0 + r / G;  // chunk-relative position
-        const bool row_ok = pos - i0 < nq;
-        const int my_last = prefix_mode ? last_key : min(start + pos, last_key);  // last key this row may see
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.f;
-        for (int j = 0; j < nt; ++j) {
-            const int st = j & 1;
-            // validity of the tile's 128 keys (inside the context, in a block with a valid table
-            // entry), published by the producer
-            if (ok && !mbar_wait(bars.m_full(j % kMaskSlots), (j / kMaskSlots) & 1)) ok = false;
-            uint32_t vm[4];
+        int gt = 0;  // key tiles taken so far
+        for (int k = blockIdx.x; k < num_items; k += gridDim.x) {
+            Item d;
+            if (!describe(k, d)) continue;
+            const int kvh = d.kvh, r0 = d.r0, start = d.start, i0 = d.i0, nq = d.nq, last_key = d.last_key, nt = d.nt;
+            const int pos = i0 + r / G;  // chunk-relative position
+            const bool row_ok = pos - i0 < nq;
+            const int my_last = prefix_mode ? last_key : min(start + pos, last_key);  // last key this row may see
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                const int g = gt + j, st = g & 1;
+                // validity of the tile's 128 keys (inside the context, in a block with a valid table
+                // entry), published by the producer
+                if (ok && !mbar_wait(bars.m_full(g % kMaskSlots), (g / kMaskSlots) & 1)) ok = false;
+                uint32_t vm[4];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) vm[w] = vmask[(j % kMaskSlots) * 4 + w];
-            if (ok && !softmax_wait(bars.s_full(st), (j >> 1) & 1)) ok = false;
-            tc_fence_after();
-            float sv[64];
+                for (int w = 0; w < 4; ++w) vm[w] = vmask[(g % kMaskSlots) * 4 + w];
+                if (ok && !softmax_wait(bars.s_full(st), (g >> 1) & 1)) ok = false;
+                tc_fence_after();
+                float sv[64];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float t[32];
-                tmem_ld32(tmem + lane_off + st * 128 + col0 + q2 * 32, t);
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float t[32];
+                    tmem_ld32(tmem + lane_off + st * 128 + col0 + q2 * 32, t);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sv[q2 * 32 + i] = t[i];
-            }
-            tmem_wait_ld();
-            const int kbase = j * kTileK + col0;
-            const uint32_t w0 = vm[half * 2], w1 = vm[half * 2 + 1];
-            // dense: every key of my 64 is valid and causally visible, and the scale is positive,
-            // so the max can be taken on raw scores and the scale folded into one FMA later
-            const bool dense = (w0 & w1) == ~0u && kbase + 63 <= my_last && sl2 > 0.f;
-            // row max over my 64 keys in eight independent chains (a single chain of 64 dependent
-            // maxima was a third of the softmax's time)
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-            if (dense) {
-#pragma unroll
-                for (int k = 0; k < 64; k += 2) mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], sv[k], sv[k + 1]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 64; ++k) {
-                    const bool valid = (((k < 32 ? w0 : w1) >> (k & 31)) & 1u) && kbase + k <= my_last;
-                    sv[k] = valid ? sv[k] * sl2 : -INFINITY;
-                    mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+                    for (int i = 0; i < 32; ++i) sv[q2 * 32 + i] = t[i];
                 }
-            }
-            float mpart = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            if (dense) mpart *= sl2;
-            const float mt = mpart;
-            if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
-                if (m_run != -INFINITY) {
-                    const float alpha = fast_exp2(m_run - mt);
-                    l_run *= alpha;
-                    if (j > 0) {
-                        // every PV issued so far (the last is PV_{j-1}) must be done before O changes
-                        if (ok && !mbar_wait(bars.o_done((j - 1) & 1), ((j - 1) >> 1) & 1)) ok = false;
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int q2 = 0; q2 < 8; ++q2) {  // all 128 columns of this half's O row
-                            float t[16];
-                            tmem_ld16(t_own + q2 * 16, t);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) t[i] *= alpha;
-                            tmem_st16(t_own + q2 * 16, t);
-                        }
-                        tmem_wait_st();
-                    }
-                }
-                m_run = mt;
-            }
-            // P = 2^(x - m) in bf16, my 64 keys of row r packed in pairs into 32 columns of S buffer j%2
-            // (its first 32 columns for keys 0-63, columns 64-95 for keys 64-127: each thread
-            // overwrites only S values it has already read)
-            float lsum = 0.f;
-            const float neg_m = -m_run;
-            {
-                uint32_t pk[32];
-                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-                if (PA_PREFILL_EXP2_PAIRS && dense) {
-                    // two keys per instruction throughout: x - m by a paired FMA, rounded to a bf16
-                    // pair, 2^x of the pair (which is P itself), and the sum of the same bf16 values
-                    // by a paired add
-                    const unsigned long long s2 = f32x2_pack(sl2, sl2), m2 = f32x2_pack(neg_m, neg_m);
-                    unsigned long long acc2[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float y0, y1;
-                        f32x2_unpack(fma_f32x2(f32x2_pack(sv[2 * i], sv[2 * i + 1]), s2, m2), y0, y1);
-                        const uint32_t e = exp2_bf16x2(pack_bf16x2(y0, y1));
-                        pk[i] = e;
-                        acc2[i & 1] = add_f32x2(
-                            acc2[i & 1], f32x2_pack(__uint_as_float(e << 16), __uint_as_float(e & 0xFFFF0000u)));
-                    }
-                    float a0, a1, b0, b1;
-                    f32x2_unpack(acc2[0], a0, a1);
-                    f32x2_unpack(acc2[1], b0, b1);
-                    ls4[0] = a0;
-                    ls4[1] = a1;
-                    ls4[2] = b0;
-                    ls4[3] = b1;
-                } else {
-                    if (dense) {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 64; ++k)
-                            sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        ls4[i & 3] += sv[2 * i] + sv[2 * i + 1];
-                        pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-                    }
-                }
-                lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-                tmem_st32u(tmem + lane_off + st * 128 + col0, pk);
-                tmem_wait_st();
-            }
-            l_run += lsum;
-            // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
-            // bytes); only then does this tile need its V to have landed here
-            const bool need_zero = (vm[0] & vm[1] & vm[2] & vm[3]) != ~0u;
-            const int vs = j % kVStages;
-            if (need_zero && ok && !mbar_wait(bars.v_full(vs), (j / kVStages) & 1)) ok = false;
-            if (need_zero && ok && half == 0 && !((vm[r >> 5] >> (r & 31)) & 1u)) {
-                uint8_t* vrow = smem + kV + vs * kTileBytes;
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4*>(vrow + h * kHalf + r * 128 + c8 * 16) = z;
-            }
-            if (need_zero) fence_proxy_async_smem();  // the zeroed rows before the PV MMA reads them
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(bars.p_full(j & 1));
-        }
-        // ---- epilogue: O / l -> out (each thread stores its 64 columns of the row)
-        if (ok && nt > 0 && !mbar_wait(bars.o_done((nt - 1) & 1), ((nt - 1) >> 1) & 1)) ok = false;
-        tc_fence_after();
-        if (!ok && lane == 0) count_error(p.error_count);
-        // combine the halves: M = max(m_a, m_b), O = (f_a O_a + f_b O_b) / (f_a l_a + f_b l_b),
-        // f_x = 2^(m_x - M); the states cross through TMEM columns 0-3 of S0 (free now)
-        tmem_st1(tmem + lane_off + half, m_run);
-        tmem_st1(tmem + lane_off + 2 + half, l_run);
-        tmem_wait_st();
-        tc_fence_before();
-        softmax_bar();
-        tc_fence_after();
-        const float m_oth = tmem_ld1(tmem + lane_off + (half ^ 1));
-        const float l_oth = tmem_ld1(tmem + lane_off + 2 + (half ^ 1));
-        tmem_wait_ld();
-        const float m_a = half ? m_oth : m_run, m_b = half ? m_run : m_oth;
-        const float l_a = half ? l_oth : l_run, l_b = half ? l_run : l_oth;
-        const float m_row = fmaxf(m_a, m_b);
-        const float f_a = m_a == -INFINITY ? 0.f : fast_exp2(m_a - m_row);
-        const float f_b = m_b == -INFINITY ? 0.f : fast_exp2(m_b - m_row);
-        const float l_row = f_a * l_a + f_b * l_b;
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        const float wa = f_a * inv, wb = f_b * inv;  // weights of O_a and O_b in this row's output
-        // member sequence r0 + pos, head r % G of a cascade prefix pass: its partial (o, m, l) goes to
-        // workspace slot 0; a member whose own prefix length differs from the group's gets an empty one
-        const int sm = r0 + pos;
-        const bool same = prefix_mode && row_ok && p.prefix_lens[sm] == start;
-        if (prefix_mode && row_ok && !same && half == 0 && r % G == 0) count_error(p.error_count);
-        const size_t slot = ((size_t)sm * p.num_kv_heads + kvh) * p.part_splits * G + (r % G);
-        if (prefix_mode && row_ok && half == 0)
-            p.part_ml[slot] = same ? make_float2(m_row, l_row) : make_float2(-INFINITY, 0.f);
-        __nv_bfloat16* out = prefix_mode ? nullptr
-                                         : static_cast<__nv_bfloat16*>(p.out) +
-                                               ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD +
-                                               col0;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // my 64 output columns, 16 at a time
-            float t[16];
-            if (nt > 0) {
-                float u[16];
-                tmem_ld16(tmem + lane_off + kTmemOa + col0 + q4 * 16, t);
-                tmem_ld16(tmem + lane_off + kTmemOb + col0 + q4 * 16, u);
                 tmem_wait_ld();
+                const int kbase = j * kTileK + col0;
+                const uint32_t w0 = vm[half * 2], w1 = vm[half * 2 + 1];
+                // dense: every key of my 64 is valid and causally visible, and the scale is positive,
+                // so the max can be taken on raw scores and the scale folded into one FMA later
+                const bool dense = (w0 & w1) == ~0u && kbase + 63 <= my_last && sl2 > 0.f;
+                // row max over my 64 keys in eight independent chains (a single chain of 64 dependent
+                // maxima was a third of the softmax's time)
+                float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) t[i] = t[i] * wa + u[i] * wb;
-            } else {
+                for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+                if (dense) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) t[i] = 0.f;
+                    for (int k = 0; k < 64; k += 2) mx8[(k >> 1) & 7] = fmax3(mx8[(k >> 1) & 7], sv[k], sv[k + 1]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) {
+                        const bool valid = (((k < 32 ? w0 : w1) >> (k & 31)) & 1u) && kbase + k <= my_last;
+                        sv[k] = valid ? sv[k] * sl2 : -INFINITY;
+                        mx8[k & 7] = fmaxf(mx8[k & 7], sv[k]);
+                    }
+                }
+                float mpart = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                if (dense) mpart *= sl2;
+                const float mt = mpart;
+                if (mt > m_run + kRescaleThreshold) {  // also true for the first finite max
+                    if (m_run != -INFINITY) {
+                        const float alpha = fast_exp2(m_run - mt);
+                        l_run *= alpha;
+                        if (j > 0) {
+                            // every PV issued so far (the last is PV_{j-1}) must be done before O changes
+                            if (ok && !mbar_wait(bars.o_done((g - 1) & 1), ((g - 1) >> 1) & 1)) ok = false;
+                            tc_fence_after();
+#pragma unroll 1
+                            for (int q2 = 0; q2 < 8; ++q2) {  // all 128 columns of this half's O row
+                                float t[16];
+                                tmem_ld16(t_own + q2 * 16, t);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) t[i] *= alpha;
+                                tmem_st16(t_own + q2 * 16, t);
+                            }
+                            tmem_wait_st();
+                        }
+                    }
+                    m_run = mt;
+                }
+                // P = 2^(x - m) in bf16, my 64 keys of row r packed in pairs into 32 columns of S buffer j%2
+                // (its first 32 columns for keys 0-63, columns 64-95 for keys 64-127: each thread
+                // overwrites only S values it has already read)
+                float lsum = 0.f;
+                const float neg_m = -m_run;
+                {
+                    uint32_t pk[32];
+                    float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (PA_PREFILL_EXP2_PAIRS && dense) {
+                        // two keys per instruction throughout: x - m by a paired FMA, rounded to a bf16
+                        // pair, 2^x of the pair (which is P itself), and the sum of the same bf16 values
+                        // by a paired add
+                        const unsigned long long s2 = f32x2_pack(sl2, sl2), m2 = f32x2_pack(neg_m, neg_m);
+                        unsigned long long acc2[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float y0, y1;
+                            f32x2_unpack(fma_f32x2(f32x2_pack(sv[2 * i], sv[2 * i + 1]), s2, m2), y0, y1);
+                            const uint32_t e = exp2_bf16x2(pack_bf16x2(y0, y1));
+                            pk[i] = e;
+                            acc2[i & 1] = add_f32x2(
+                                acc2[i & 1], f32x2_pack(__uint_as_float(e << 16), __uint_as_float(e & 0xFFFF0000u)));
+                        }
+                        float a0, a1, b0, b1;
+                        f32x2_unpack(acc2[0], a0, a1);
+                        f32x2_unpack(acc2[1], b0, b1);
+                        ls4[0] = a0;
+                        ls4[1] = a1;
+                        ls4[2] = b0;
+                        ls4[3] = b1;
+                    } else {
+                        if (dense) {
+#pragma unroll
+                            for (int k = 0; k < 64; ++k) sv[k] = fast_exp2(fmaf(sv[k], sl2, neg_m));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 64; ++k)
+                                sv[k] = (sv[k] == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(sv[k] + neg_m);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            ls4[i & 3] += sv[2 * i] + sv[2 * i + 1];
+                            pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+                        }
+                    }
+                    lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+                    tmem_st32u(tmem + lane_off + st * 128 + col0, pk);
+                    tmem_wait_st();
+                }
+                l_run += lsum;
+                // V rows that carry no valid key for any query row are zeroed (stale or non-finite pool
+                // bytes); only then does this tile need its V to have landed here
+                const bool need_zero = (vm[0] & vm[1] & vm[2] & vm[3]) != ~0u;
+                const int vs = g % kVStages;
+                if (need_zero && ok && !mbar_wait(bars.v_full(vs), (g / kVStages) & 1)) ok = false;
+                if (need_zero && ok && half == 0 && !((vm[r >> 5] >> (r & 31)) & 1u)) {
+                    uint8_t* vrow = smem + kV + vs * kTileBytes;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) *reinterpret_cast<uint4*>(vrow + h * kHalf + r * 128 + c8 * 16) = z;
+                }
+                if (need_zero) fence_proxy_async_smem();  // the zeroed rows before the PV MMA reads them
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(bars.p_full(st));
             }
-            if (!row_ok) continue;
-            if (prefix_mode) {
-                float4* po = reinterpret_cast<float4*>(p.part_o + slot * kD + col0 + q4 * 16);
-                const float f = same ? 1.f : 0.f;
+            // ---- epilogue: O / l -> out (each thread stores its 64 columns of the row)
+            const int g_last = gt + nt - 1;
+            if (ok && nt > 0 && !mbar_wait(bars.o_done(g_last & 1), (g_last >> 1) & 1)) ok = false;
+            tc_fence_after();
+            // combine the halves: M = max(m_a, m_b), O = (f_a O_a + f_b O_b) / (f_a l_a + f_b l_b),
+            // f_x = 2^(m_x - M); the states cross through TMEM columns 0-3 of S0 (free now: the MMA warp
+            // starts the next item only after o_free)
+            // (an item without keys has no state to combine and must not touch tensor memory, which the MMA
+            // warp may already be filling for the next item)
+            float m_oth = -INFINITY, l_oth = 0.f;
+            if (nt > 0) {
+                tmem_st1(tmem + lane_off + half, m_run);
+                tmem_st1(tmem + lane_off + 2 + half, l_run);
+                tmem_wait_st();
+                tc_fence_before();
+                softmax_bar();
+                tc_fence_after();
+                m_oth = tmem_ld1(tmem + lane_off + (half ^ 1));
+                l_oth = tmem_ld1(tmem + lane_off + 2 + (half ^ 1));
+                tmem_wait_ld();
+            }
+            const float m_a = half ? m_oth : m_run, m_b = half ? m_run : m_oth;
+            const float l_a = half ? l_oth : l_run, l_b = half ? l_run : l_oth;
+            const float m_row = fmaxf(m_a, m_b);
+            const float f_a = m_a == -INFINITY ? 0.f : fast_exp2(m_a - m_row);
+            const float f_b = m_b == -INFINITY ? 0.f : fast_exp2(m_b - m_row);
+            const float l_row = f_a * l_a + f_b * l_b;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            const float wa = f_a * inv, wb = f_b * inv;  // weights of O_a and O_b in this row's output
+            // member sequence r0 + pos, head r % G of a cascade prefix pass: its partial (o, m, l) goes to
+            // workspace slot 0; a member whose own prefix length differs from the group's gets an empty one
+            const int sm = r0 + pos;
+            const bool same = prefix_mode && row_ok && p.prefix_lens[sm] == start;
+            if (prefix_mode && row_ok && !same && half == 0 && r % G == 0) count_error(p.error_count);
+            const size_t slot = ((size_t)sm * p.num_kv_heads + kvh) * p.part_splits * G + (r % G);
+            if (prefix_mode && row_ok && half == 0)
+                p.part_ml[slot] = same ? make_float2(m_row, l_row) : make_float2(-INFINITY, 0.f);
+            __nv_bfloat16* out = prefix_mode ? nullptr
+                                             : static_cast<__nv_bfloat16*>(p.out) +
+                                                   ((size_t)(r0 + pos) * p.num_q_heads + (size_t)kvh * G + (r % G)) * kD +
+                                                   col0;
 #pragma unroll
-                for (int i = 0; i < 16; i += 4)
-                    po[i / 4] = make_float4(t[i] * f, t[i + 1] * f, t[i + 2] * f, t[i + 3] * f);
-            } else {
+            for (int q4 = 0; q4 < 4; ++q4) {  // my 64 output columns, 16 at a time
+                float t[16];
+                if (nt > 0) {
+                    float u[16];
+                    tmem_ld16(tmem + lane_off + kTmemOa + col0 + q4 * 16, t);
+                    tmem_ld16(tmem + lane_off + kTmemOb + col0 + q4 * 16, u);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; i += 8) {
-                    uint4 pk;
-                    pk.x = pack_bf16x2(t[i], t[i + 1]);
-                    pk.y = pack_bf16x2(t[i + 2], t[i + 3]);
-                    pk.z = pack_bf16x2(t[i + 4], t[i + 5]);
-                    pk.w = pack_bf16x2(t[i + 6], t[i + 7]);
-                    *reinterpret_cast<uint4*>(out + q4 * 16 + i) = pk;
+                    for (int i = 0; i < 16; ++i) t[i] = t[i] * wa + u[i] * wb;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) t[i] = 0.f;
+                }
+                if (!row_ok) continue;
+                if (prefix_mode) {
+                    float4* po = reinterpret_cast<float4*>(p.part_o + slot * kD + col0 + q4 * 16);
+                    const float f = same ? 1.f : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        po[i / 4] = make_float4(t[i] * f, t[i + 1] * f, t[i + 2] * f, t[i + 3] * f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i += 8) {
+                        uint4 pk;
+                        pk.x = pack_bf16x2(t[i], t[i + 1]);
+                        pk.y = pack_bf16x2(t[i + 2], t[i + 3]);
+                        pk.z = pack_bf16x2(t[i + 4], t[i + 5]);
+                        pk.w = pack_bf16x2(t[i + 6], t[i + 7]);
+                        *reinterpret_cast<uint4*>(out + q4 * 16 + i) = pk;
+                    }
                 }
             }
+            if (nt > 0) {  // O has been read: the MMA warp may start the next item
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && ok) mbar_arrive(bars.o_free());
+            }
+            gt += nt;
         }
+        if (!ok && lane == 0) count_error(p.error_count);
     }
     tc_fence_before();
     __syncthreads();
@@ -594,9 +676,17 @@ int launch_prefill_tc(const PrefillParams& p, cudaStream_t stream) {
     if (rc != PA_OK) return rc;
     if ((rc = pool_tensor_map(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, kD)) != PA_OK) return rc;
     if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_tc_kernel), kSmemBytes)) != PA_OK) return rc;
+    // persistent: one CTA per SM (or per work item, if fewer), each walking its share of the items
     const int pos_per_tile = kTileQ / p.group;
-    dim3 grid((p.max_q_len + pos_per_tile - 1) / pos_per_tile, p.num_kv_heads, p.num_chunks);
-    return launch_kernel(prefill_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, tmq, tmk, tmv, p);
+    const long long items = (long long)((p.max_q_len + pos_per_tile - 1) / pos_per_tile) * p.num_chunks *
+                            p.num_kv_heads;
+    if (items == 0) return PA_OK;
+    int dev = 0, num_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return check_launch();
+    const int grid = (int)(items < num_sms ? items : num_sms);
+    return launch_kernel(prefill_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, tmq, tmk, tmv, p);
 }
 
 }  // namespace pa
