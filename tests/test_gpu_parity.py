@@ -258,6 +258,31 @@ def test_prefill_shapes(case):
     assert st.errors() == 0
 
 
+PREFILL_RAGGED_CASES = [
+    # (Hq, Hkv, B): many chunks of ragged lengths (one empty, single queries, a full 512) at scattered offsets,
+    # so the persistent prefill grid walks several passes of items, most of them partial tiles
+    (32, 8, 16),
+    (64, 8, 64),
+    (8, 8, 128),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_RAGGED_CASES)))
+def test_prefill_many_ragged_chunks(case):
+    Hq, Hkv, B = PREFILL_RAGGED_CASES[case]
+    lens = [1, 0, 200, 33, 129, 7, 512, 64, 300, 5, 1, 96]
+    offs = [0, 10, 700, 0, 2000, 64, 0, 3000, 1, 31, 4095, 128]
+    w = W.prefill_batch(160 + case, Hq, Hkv, 128, B, lens, offs, dtype=torch.bfloat16, decode_lens=[3, 900])
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    err = _maxabs(st.out_prefill, exp.out_prefill)
+    assert err <= TOL[torch.bfloat16], f"prefill max-abs error {err}"
+    assert _maxabs(st.out_decode, exp.out_decode) <= TOL[torch.bfloat16]
+    assert st.errors() == 0
+
+
 def test_graph_replay_matches_eager():
     """The captured step (CUDA graph of the four library calls) gives the same
     outputs as eager calls, replay after replay."""
