@@ -62,10 +62,6 @@ namespace {
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 3
 #endif
-// Waits that poll before sleeping (bit 0: the producer's free-slot waits, bit 1: the consumers' data waits).
-#ifndef PA_DECODE_SPIN
-#define PA_DECODE_SPIN 0
-#endif
 #ifndef PA_DECODE_CLAIM_STAGES
 #define PA_DECODE_CLAIM_STAGES 2
 #endif
@@ -367,7 +363,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     if (skip > 0) lvalid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
                 }
                 if (stage_no >= (uint32_t)C::kStages &&
-                    !(PA_DECODE_SPIN & 1 ? mbar_wait_spin : mbar_wait)(&empty[slot], ((stage_no / C::kStages) - 1) & 1)) {
+                    !mbar_wait(&empty[slot], ((stage_no / C::kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -476,7 +472,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
         const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kSegs * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
             const int slot = stage_no % C::kStages;
-            if (!(PA_DECODE_SPIN & 2 ? mbar_wait_spin : mbar_wait)(&full[slot], (stage_no / C::kStages) & 1)) {
+            if (!mbar_wait(&full[slot], (stage_no / C::kStages) & 1)) {
                 if (lane == 0) count_error(p.error_count);
                 break;
             }

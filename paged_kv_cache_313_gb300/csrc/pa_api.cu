@@ -85,6 +85,10 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 // Items per SM below which decode partitions shrink from 512 to 256 and 128
 // tokens (build-time knob; 0, the measured best, keeps 512 whenever the grid
 // covers two waves: shorter items spend more of their time in the epilogue).
+// Longest decode partition (tokens per work item) before any shrinking.
+#ifndef PA_DECODE_PARTITION
+#define PA_DECODE_PARTITION 512
+#endif
 #ifndef PA_DECODE_ITEMS_PER_SM
 #define PA_DECODE_ITEMS_PER_SM 0
 #endif
@@ -102,7 +106,7 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         long long splits = ((long long)max_context_len + part - 1) / part;
         return (long long)num_seqs * num_kv_heads * (splits < 1 ? 1 : splits);
     };
-    int partition = 512;
+    int partition = PA_DECODE_PARTITION;
     while (partition > 128 && items(partition) < (long long)PA_DECODE_ITEMS_PER_SM * num_sms) partition >>= 1;
     while (partition > 64 && items(partition) < 2LL * num_sms) partition >>= 1;
     auto splits_of = [&](int part) {

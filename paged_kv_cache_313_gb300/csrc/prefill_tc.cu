@@ -77,22 +77,6 @@ constexpr int kTmemSlot = kMask + kMaskSlots * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
-// The MMA-issuing thread waits by polling (it sits on the critical path of
-// every tile: a sleeping wait noticed the softmax's P about 750 cycles after
-// the last warp arrived); the softmax warps optionally too (build knobs).
-#ifndef PA_PREFILL_MMA_SPIN
-#define PA_PREFILL_MMA_SPIN 0
-#endif
-#ifndef PA_PREFILL_SOFTMAX_SPIN
-#define PA_PREFILL_SOFTMAX_SPIN 0
-#endif
-__device__ __forceinline__ bool mma_wait(uint64_t* bar, uint32_t parity) {
-    return PA_PREFILL_MMA_SPIN ? mbar_wait_spin(bar, parity) : mbar_wait(bar, parity);
-}
-__device__ __forceinline__ bool softmax_wait(uint64_t* bar, uint32_t parity) {
-    return PA_PREFILL_SOFTMAX_SPIN ? mbar_wait_spin(bar, parity) : mbar_wait(bar, parity);
-}
-
 // Dense tiles exponentiate in bf16 pairs (one instruction per two keys; P is
 // rounded to bf16 for its MMA either way, the pair form also rounds x - m).
 #ifndef PA_PREFILL_EXP2_PAIRS
@@ -333,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the loop with warp-uniform descriptors; one elected lane issues every
         // MMA and commit.  (Run by lane 0 alone, the same loop spent about 75 cycles per MMA issued.)
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mma_wait(bar, parity)) != 0;
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
         };
         constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
         constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
@@ -434,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t vm[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) vm[w] = vmask[(g % kMaskSlots) * 4 + w];
-                if (ok && !softmax_wait(bars.s_full(st), (g >> 1) & 1)) ok = false;
+                if (ok && !mbar_wait(bars.s_full(st), (g >> 1) & 1)) ok = false;
                 tc_fence_after();
                 float sv[64];
 #pragma unroll
