@@ -85,9 +85,9 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 // Items per SM below which decode partitions shrink from 512 to 256 and 128
 // tokens (build-time knob; 0, the measured best, keeps 512 whenever the grid
 // covers two waves: shorter items spend more of their time in the epilogue).
-// Longest decode partition (tokens per work item) before any shrinking.
+// Decode partition (tokens per work item) before any shrinking or growing.
 #ifndef PA_DECODE_PARTITION
-#define PA_DECODE_PARTITION 512
+#define PA_DECODE_PARTITION 1024
 #endif
 #ifndef PA_DECODE_ITEMS_PER_SM
 #define PA_DECODE_ITEMS_PER_SM 0
@@ -95,8 +95,10 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
                        int num_sms, size_t workspace_cap) {
-    // Work items are (sequence, partition, kv head).  512-token partitions
-    // keep each item's stream of K/V long; shrink them while the batch would
+    // Work items are (sequence, partition, kv head).  PA_DECODE_PARTITION-token
+    // partitions (1024: measured against 512 and 2048, it halves the partials
+    // a long context leaves to merge and is neutral elsewhere) keep each item's
+    // stream of K/V long; shrink them while the batch would
     // give fewer than PA_DECODE_ITEMS_PER_SM items per SM (if set) and while
     // the grid would not cover two waves of the GPU; grow them so
     // that no (sequence, head) has more than 128 partials to merge and the

@@ -219,8 +219,8 @@ PREFILL_CASES = [
 
 DECODE_SHAPE_CASES = [
     # (Hq, Hkv, D, B, decode context lengths, dtype): tensor-core decode at head_dim 64 and 128, every block
-    # size it takes and groups 1..8, partition boundaries (63/64/65, 512/513), and the CUDA-core path for
-    # group 16 and fp32
+    # size it takes and groups 1..8, stage and partition boundaries (63/64/65, 512/513, 1025, 4097), and the
+    # CUDA-core path for group 16 and fp32
     (8, 8, 64, 16, [1, 63, 64, 65, 700, 1300], torch.bfloat16),
     (16, 8, 64, 8, [5, 512, 513, 2000], torch.bfloat16),
     (64, 8, 128, 64, [1, 100, 4097], torch.bfloat16),
@@ -326,11 +326,11 @@ def test_run_from_host_matches_device_step():
 
 def test_decode_plan_matches_workspace_and_launches():
     """The plan reported through the ABI is the one pa_decode sizes its
-    workspace for: 512-token partitions on the bf16 decode workload (64
+    workspace for: 1024-token partitions on the bf16 decode workload (64
     sequences, 8 kv heads, contexts up to 4096) and one partition (no merge
     kernel) for a context that fits one."""
     part, splits = pa.pa_decode_plan(64, 32, 8, 128, 16, 4096)
-    assert (part, splits) == (512, 8)
+    assert (part, splits) == (1024, 4)
     need = pa.pa_decode_workspace_size(64, 32, 8, 128, 16, 4096)
     assert need >= 64 * 8 * splits * 4 * 128 * 4
     part1, splits1 = pa.pa_decode_plan(512, 32, 8, 128, 16, 300)
