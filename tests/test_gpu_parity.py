@@ -145,6 +145,31 @@ def test_long_single_sequence_fp32_many_partitions():
     assert _maxabs(got, want) <= 1e-5
 
 
+@pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-6), (torch.bfloat16, 1e-2)])
+def test_split_count_does_not_change_the_result(dtype, tol):
+    """The split-KV merge is exact up to rounding: one sequence decoded alone (its plan shrinks the partitions
+    to cover the GPU: 64-token partitions, about 47 partials to merge) and as one member of a 64-sequence
+    batch (1024-token partitions, 3 partials) agree within `tol`."""
+    rng = np.random.default_rng(12)
+    N, L, B, Hq, Hkv, D = 64, 3000, 16, 8, 2, 128
+    nblk = oracle.num_blocks(L, B)
+    P = N * nblk + 9
+    tables = rng.permutation(P)[:N * nblk].astype(np.int32).reshape(N, nblk)
+    kc = torch.from_numpy(rng.standard_normal((P, B, Hkv, D), dtype=np.float32)).to(dtype).cuda()
+    vc = torch.from_numpy(rng.standard_normal((P, B, Hkv, D), dtype=np.float32)).to(dtype).cuda()
+    q = torch.from_numpy(rng.standard_normal((N, Hq, D), dtype=np.float32)).to(dtype).cuda()
+    lens = torch.from_numpy(rng.integers(1, L + 1, size=N).astype(np.int32))
+    lens[5] = L
+    bt, ctx = torch.from_numpy(tables).cuda(), lens.cuda()
+    part_one, splits_one = pa.pa_decode_plan(1, Hq, Hkv, D, B, L)
+    part_all, splits_all = pa.pa_decode_plan(N, Hq, Hkv, D, B, L)
+    assert splits_one > 10 * splits_all > 10
+    alone = _decode_direct(q[5:6].contiguous(), kc, vc, bt[5:6].contiguous(), ctx[5:6].contiguous(), L, 0.09)
+    batch = _decode_direct(q, kc, vc, bt, ctx, L, 0.09)
+    torch.cuda.synchronize()
+    assert float((alone[0].float() - batch[5].float()).abs().max()) <= tol
+
+
 def test_empty_and_single_token_contexts():
     rng = np.random.default_rng(3)
     P, B, Hq, Hkv, D = 8, 16, 8, 2, 128
