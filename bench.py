@@ -403,7 +403,8 @@ def run_native(args):
     prefill_ms = [e[2].elapsed_time(e[3]) for e in kev]
 
     # ---- end to end through the public API: the packed inputs copied in from
-    # pinned host memory (one copy), the step, the packed outputs copied back
+    # pinned host memory (one copy), then the step, whose kernels store the
+    # outputs straight into a pinned host buffer (d2h: those output bytes)
     host_in = step.pinned_inputs()
     host_out = step.pinned_outputs()
     step.step_from_host(host_in, host_out)

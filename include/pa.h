@@ -21,7 +21,11 @@
  * Conventions for every entry point:
  *  - Tensor arguments are DEVICE pointers owned by the caller, contiguous,
  *    row-major.  The library allocates no device memory; scratch comes from
- *    the caller's workspace.
+ *    the caller's workspace.  An attention output (`out`) may instead be
+ *    page-locked host memory mapped into the device's address space (as
+ *    cudaHostAlloc gives on this platform): the kernels then store the
+ *    results straight into host memory, visible to the host once the stream
+ *    has been synchronised.
  *  - K and V pools are separate arrays laid out [num_blocks][block_size]
  *    [num_kv_heads][head_dim]: element (slot, h, d) is at
  *    (slot*num_kv_heads + h)*head_dim + d.  Query head h reads KV head

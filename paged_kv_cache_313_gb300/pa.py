@@ -94,11 +94,13 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
 
 
-def _dev(t: torch.Tensor | None, name: str, dtype=None):
+def _dev(t: torch.Tensor | None, name: str, dtype=None, host_ok: bool = False):
+    """Pointer of a contiguous CUDA tensor (or, with host_ok, of a pinned host tensor, which the device reaches
+    through its mapping)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -212,7 +214,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len: 
     if out is None:
         out = torch.empty_like(q)
     _check("pa_decode", lib().pa_decode(
-        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(out, "out", q.dtype, host_ok=True),
+        _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -232,7 +235,8 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_l
     if out is None:
         out = torch.empty_like(q)
     _check("pa_decode_fp8", lib().pa_decode_fp8(
-        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), N, Hq, Hkv, D, _dev(k_cache, "k_cache"),
+        _dev(out, "out", torch.bfloat16, host_ok=True),
+        _dev(q, "q", torch.bfloat16), N, Hq, Hkv, D, _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), P, B, _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale), float(k_scale),
         float(v_scale), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -251,7 +255,8 @@ def pa_decode_write(q, k_cache, v_cache, block_tables, context_lens, max_context
     if out is None:
         out = torch.empty_like(q)
     _check("pa_decode_write", lib().pa_decode_write(
-        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(out, "out", q.dtype, host_ok=True),
+        _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype), _dev(new_slots, "new_slots", torch.int64),
@@ -283,7 +288,8 @@ def pa_decode_cascade(q, k_cache, v_cache, block_tables, context_lens, max_conte
         out = torch.empty_like(q)
     G = group_offsets.numel() - 1
     _check("pa_decode_cascade", lib().pa_decode_cascade(
-        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(out, "out", q.dtype, host_ok=True),
+        _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len),
         _dev(group_offsets, "group_offsets", torch.int32), G, int(max_group_size),
@@ -306,7 +312,8 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_conte
     if out is None:
         out = torch.empty_like(q)
     _check("pa_decode_noalloc", lib().pa_decode_noalloc(
-        _dev(out, "out", q.dtype), _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
+        _dev(out, "out", q.dtype, host_ok=True),
+        _dev(q, "q"), N, Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
@@ -332,7 +339,7 @@ def pa_prefill_chunk(q, cu_q_lens, q_start_pos, seq_of_chunk, max_q_len: int, k_
     ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("pa_prefill_chunk", lib().pa_prefill_chunk(
-        _dev(out, "out", q.dtype), _dev(q, "q"), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        _dev(out, "out", q.dtype, host_ok=True), _dev(q, "q"), _dev(cu_q_lens, "cu_q_lens", torch.int32),
         _dev(q_start_pos, "q_start_pos", torch.int32), _dev(seq_of_chunk, "seq_of_chunk", torch.int32), C, T,
         int(max_q_len), block_tables.shape[0], Hq, Hkv, D, _dtype_code(q), _dev(k_cache, "k_cache", q.dtype),
         _dev(v_cache, "v_cache", q.dtype), P, B, _dev(block_tables, "block_tables", torch.int32),

@@ -206,19 +206,36 @@ class DeviceStep:
         _, views = _packed_views(host_out, [self.out_decode, self.out_prefill])
         return views
 
+    # outputs up to this size are stored by the step's kernels straight into pinned host memory; larger ones
+    # (a prefill batch's) are written to device memory and copied out, since kernels storing tens of megabytes
+    # across the host link were measured to slow down more than the copy costs
+    DIRECT_OUTPUT_BYTES = 4 << 20
+
     def step_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor, stream=None):
         """One step from pinned host memory, eagerly: the packed inputs copied in
-        by a kernel reading the pinned buffer (pa_stage_copy), the step, the
-        packed outputs copied back the same way."""
+        by a kernel reading the pinned buffer (pa_stage_copy), then the step,
+        whose kernels store each small output straight into the pinned output
+        buffer through its device mapping; a large output is copied out after
+        the step."""
         pa.pa_stage_copy(self.inbuf, host_in, stream=stream)
-        self.run(stream)
-        pa.pa_stage_copy(host_out, self.outbuf, stream=stream)
+        dev_out = (self.out_decode, self.out_prefill)
+        host_views = self.output_views(host_out)
+        direct = [t.numel() * t.element_size() <= self.DIRECT_OUTPUT_BYTES for t in dev_out]
+        self.out_decode, self.out_prefill = (h if d else t for h, t, d in zip(host_views, dev_out, direct))
+        try:
+            self.run(stream)
+        finally:
+            self.out_decode, self.out_prefill = dev_out
+        for h, t, d in zip(host_views, dev_out, direct):
+            if not d and t.numel():
+                pa.pa_stage_copy(h, t, stream=stream)
         return host_out
 
     def capture_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor) -> "torch.cuda.CUDAGraph":
-        """Record copy-in, step and copy-out as one CUDA graph bound to these two
-        pinned buffers: a serving loop writes the next step's inputs into
-        host_in, replays, and reads host_out.  Call after one eager step."""
+        """Record copy-in and the step (writing into host_out) as one CUDA graph
+        bound to these two pinned buffers: a serving loop writes the next step's
+        inputs into host_in, replays, and reads host_out once the stream is
+        synchronised.  Call after one eager step."""
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(side):
@@ -231,8 +248,8 @@ class DeviceStep:
         return g
 
     def run_from_host(self, host_in: torch.Tensor, host_out: torch.Tensor, graph: bool = True):
-        """One step from pinned host memory: copy the packed inputs in, run the
-        step, copy the packed outputs back — the captured graph of
+        """One step from pinned host memory: copy the packed inputs in and run the
+        step with its outputs stored into host_out — the captured graph of
         capture_from_host when `graph` and it was captured for these buffers,
         else eagerly.  Asynchronous on the current stream."""
         hg = getattr(self, "host_graph", None)
