@@ -8,12 +8,14 @@
 // h/G, out = softmax_j(scale q.k_j) v_j over the sequence's context.
 //
 // Work decomposition.  A work item is (sequence, partition of its context,
-// kv head); partitions are `partition` tokens (a multiple of 64).  Items are
-// numbered densely, sequence-major then partition then kv head, from a
-// prefix sum of the per-sequence item counts that every CTA computes once
-// from context_lens.  Persistent CTAs (two per SM for bf16 pools, three for
-// e4m3 pools) take items from a global counter in the workspace, so long and
-// short sequences balance dynamically.
+// kv head) — or, for e4m3 pools with an even number of kv heads, a pair of
+// adjacent kv heads, whose rows sit side by side in the pool so that one box
+// per block carries both; partitions are `partition` tokens (a multiple of
+// 64).  Items are numbered densely, sequence-major then partition then kv
+// head, from a prefix sum of the per-sequence item counts that every CTA
+// computes once from context_lens.  Persistent CTAs (two per SM; three for
+// single-head e4m3 items) take items from a global counter in the workspace,
+// so long and short sequences balance dynamically.
 //
 // Inside a CTA:
 //  * Warp 4 is the producer.  For each 64-token stage it waits for a free
@@ -33,7 +35,8 @@
 //    runs dry.  Boxes land 128-byte swizzled (ldmatrix reads are bank-conflict
 //    free) in a ring of kStages stages, completion counted on mbarriers; the
 //    producer streams straight across item boundaries.
-//  * Warps 0-3 consume 16 tokens of each stage apiece.  The G <= 8 query
+//  * Warps 0-3 consume 16 tokens of each stage apiece (two-head items: warps
+//    0-1 take the first head and 2-3 the second, 32 tokens apiece).  The G <= 8 query
 //    heads form the N=8 side of m16n8k16 tensor-core MMAs:
 //        S^T[16 tok x 8 heads] = K[16 tok x D] . Q^T        (D/16 MMAs)
 //        O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T       (D/16 MMAs)
@@ -45,8 +48,8 @@
 //  * Tokens past the context or in blocks with an invalid table entry are
 //    masked (score -inf) and their V rows zeroed before the PV MMA, so stale
 //    or non-finite pool contents never reach the output.
-//  * On an item's last stage the consumers combine their four states through
-//    slabs in the K tile of the stage just consumed and write the output (one
+//  * On an item's last stage the consumers combine their states (per kv head)
+//    through slabs in the K tile of the stage just consumed and write the output (one
 //    partition) or a partial for the split-KV merge kernel (decode_merge.cu);
 //    no fence, ticket or wait on other CTAs.  The producer keeps filling the
 //    other stages of the ring meanwhile.
@@ -790,7 +793,8 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 acc.z *= sc;
                 acc.w *= sc;
                 if (inf.flags & 4) {
-                    *reinterpret_cast<uint2*>(out + idx) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+                    *reinterpret_cast<uint2*>(out + idx) =
+                        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
                 } else {
                     *reinterpret_cast<float4*>(wo) = acc;
                     if (dc == 0) p.ws_ml[slot_ws * G + h] = make_float2(M, Ls);
@@ -839,8 +843,8 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * resident;
     int grid = (int)(max_items < slots ? max_items : slots);
-    return launch_kernel(decode_tc_kernel<D, kFp8, kPair>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tmk, tmv,
-                         p, p.work);
+    return launch_kernel(decode_tc_kernel<D, kFp8, kPair>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
+                         tmk, tmv, p, p.work);
 }
 
 }  // namespace
