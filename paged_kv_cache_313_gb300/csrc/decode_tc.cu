@@ -24,7 +24,8 @@
 //    a physical block of one kv head is B rows of head_dim contiguous
 //    elements at a row stride of Hkv*head_dim, one box {128 bytes, B rows,
 //    row bytes/128 segments} of the pool viewed as [128-byte segment][row]
-//    [128 bytes] — from separate lanes, so the boxes go out together; on an
+//    [128 bytes] — from separate lanes, so the boxes go out together (with an
+//    L2 evict-first policy: each K/V byte is read once per call); on an
 //    item's first stage it adds a 1-D bulk copy of the item's G query rows.
 //    Everything else is off the per-stage path: the next item is claimed two
 //    stages before the current one's last and described (with its first 32
@@ -64,6 +65,10 @@ namespace {
 // Ring depth and CTAs per SM (build-time knobs; the defaults are the measured best).
 #ifndef PA_DECODE_STAGES
 #define PA_DECODE_STAGES 3
+#endif
+// K/V copies tagged evict-first in L2 (they are read once; tables, queries and partials stay).
+#ifndef PA_DECODE_KV_EVICT_FIRST
+#define PA_DECODE_KV_EVICT_FIRST 1
 #endif
 #ifndef PA_DECODE_CLAIM_STAGES
 #define PA_DECODE_CLAIM_STAGES 2
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
         const int bps = C::kStageTok / B;   // blocks per stage (B <= 64)
         const int spc = 32 / bps;           // stages per 32-block chunk of the table
         const uint32_t block_bytes = 2u * C::kSegs * B * 128u;  // K and V of one block and the item's kv heads
+        const uint64_t kv_policy = l2_policy_evict_first();  // K/V is read once per call
 
         int item = 0;
         if (lane == 0) item = atomicAdd(&work[0], 1);
@@ -424,8 +430,12 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 const int b = lane - isv * nbs;
                 const int my_pb = __shfl_sync(0xffffffffu, pb_lane, (b0 + (lane < 2 * nbs ? b : 0)) & 31);
                 if (lane < 2 * nbs && my_pb >= 0)
-                    tma_load_3d(kdst + isv * C::kTileBytes + b * C::kSegs * B * 128, isv ? &tmv : &tmk, 0,
-                                my_pb * B, d.kvh * C::kHalves, &full[slot]);
+                    if (PA_DECODE_KV_EVICT_FIRST)
+                        tma_load_3d_hint(kdst + isv * C::kTileBytes + b * C::kSegs * B * 128, isv ? &tmv : &tmk, 0,
+                                         my_pb * B, d.kvh * C::kHalves, &full[slot], kv_policy);
+                    else
+                        tma_load_3d(kdst + isv * C::kTileBytes + b * C::kSegs * B * 128, isv ? &tmv : &tmk, 0,
+                                    my_pb * B, d.kvh * C::kHalves, &full[slot]);
                 __syncwarp();
                 ++stage_no;
                 if (st == claim_at && lane == 0) nxt = atomicAdd(&work[0], 1);
