@@ -180,7 +180,8 @@ def longctx_bf16(seed: int = 0, num_seqs: int = 16, min_len: int = 1024, max_len
 
 
 def shared_prefix_bf16(seed: int = 0, num_prompts: int = 32, branches: int = 8, prefix_len: int = 2048,
-                       max_tail: int = 512, B: int = 16, name: str = "shared_prefix_bf16") -> Workload:
+                       max_tail: int = 512, B: int = 16, name: str = "shared_prefix_bf16", num_q_heads: int = 32,
+                       num_kv_heads: int = 8) -> Workload:
     """Parallel sampling: each prompt's prefix blocks are shared (ref-counted) by its
     branches; each branch then adds a private tail of U{0..max_tail} tokens and one
     new token.  A prefix that ends inside a block makes each branch's first write
@@ -205,7 +206,8 @@ def shared_prefix_bf16(seed: int = 0, num_prompts: int = 32, branches: int = 8, 
     vrng = np.random.default_rng(seed)
     meta = {"prefix_len": prefix_len, "num_prompts": num_prompts, "branches": branches,
             "unique_tokens": num_prompts * prefix_len + int(tails.sum()) + num_prompts * branches}
-    return _finish(name, torch.bfloat16, 32, 8, 128, B, alloc, vrng, seqs, lens, cow=cow, meta=meta)
+    return _finish(name, torch.bfloat16, num_q_heads, num_kv_heads, 128, B, alloc, vrng, seqs, lens, cow=cow,
+                   meta=meta)
 
 
 def as_fp8(w: Workload, seed: int, k_scale: float = 1.0 / 64, v_scale: float = 1.0 / 64, lo: int = 0x30,

@@ -61,6 +61,12 @@ def test_host_side_rejections_need_no_device(lib):
     assert lib.pa_decode_plan(-1, 8, 8, 128, 16, 100, None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode_plan(4, 3, 2, 128, 16, 100, None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_decode_plan(4, 8, 8, 96, 16, 100, None, None) == pa.PA_ERR_UNSUPPORTED
+    # cascade decode is bf16 only, and takes the decode kernel's head sizes only
+    cas = [None, None, 4, 32, 8, 128, pa.PA_F32, None, None, 10, 16, None, 4, None, 100, None, 1, 4, None,
+           ctypes.c_float(1.0), None, 0, None, None]
+    assert lib.pa_decode_cascade(*cas) == pa.PA_ERR_UNSUPPORTED
+    cas[5], cas[6] = 96, pa.PA_BF16
+    assert lib.pa_decode_cascade(*cas) == pa.PA_ERR_UNSUPPORTED
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 0, None, None) == pa.PA_OK
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 2, None, None) == \
         pa.PA_ERR_INVALID_ARG

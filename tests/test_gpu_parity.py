@@ -283,6 +283,28 @@ def test_prefill_shapes(case):
     assert st.errors() == 0
 
 
+PREFILL_FALLBACK_CASES = [
+    # (Hq, Hkv, D, B, chunk_lens, offsets, dtype): shapes the tensor-core prefill does not take (16 query heads
+    # per kv head, head_dim 64), served by the CUDA-core prefill kernel
+    (32, 2, 128, 16, [70, 1, 130], [3, 0, 300], torch.bfloat16),
+    (16, 4, 64, 32, [200, 33], [0, 517], torch.bfloat16),
+    (8, 8, 64, 16, [65, 9], [100, 0], torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL_FALLBACK_CASES)))
+def test_prefill_fallback_shapes(case):
+    Hq, Hkv, D, B, lens, offs, dt = PREFILL_FALLBACK_CASES[case]
+    w = W.prefill_batch(140 + case, Hq, Hkv, D, B, lens, offs, dtype=dt, decode_lens=[2, 150])
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert _maxabs(st.out_prefill, exp.out_prefill) <= TOL[dt]
+    assert _maxabs(st.out_decode, exp.out_decode) <= TOL[dt]
+    assert st.errors() == 0
+
+
 PREFILL_RAGGED_CASES = [
     # (Hq, Hkv, B): many chunks of ragged lengths (one empty, single queries, a full 512) at scattered offsets,
     # so the persistent prefill grid walks several passes of items, most of them partial tiles
@@ -388,6 +410,27 @@ def test_cascade_decode_matches_oracle_and_plain_decode(prefix_len, B):
     again = cas.decode()
     torch.cuda.synchronize()
     assert torch.equal(again, got)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (8, 8), (16, 4)])
+def test_cascade_decode_every_head_group(Hq, Hkv):
+    """Cascade decode with 8, 1 and 4 query heads per kv head: a group's tile holds 32 / G members' rows, so
+    with G = 8 the five branches of a prompt split into groups of four and one, and with G = 1 they share one
+    five-row tile.  Against the oracle and against plain decode of the same batch."""
+    w = W.shared_prefix_bf16(11, num_prompts=3, branches=5, prefix_len=100, max_tail=60, B=16, name="cascade_heads",
+                             num_q_heads=Hq, num_kv_heads=Hkv)
+    exp = expected_step(w)
+    cas = DeviceStep(w)
+    assert cas.use_cascade
+    cas.slot_mapping()
+    cas.write_kv()
+    got = cas.decode().clone()
+    plain = DeviceStep(w, cascade=False)
+    plain.run()
+    torch.cuda.synchronize()
+    assert cas.errors() == 0 and plain.errors() == 0
+    assert _maxabs(got, exp.out_decode) <= TOL[w.dtype]
+    assert (got.float() - plain.out_decode.float()).abs().max().item() <= TOL[w.dtype]
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "mixed_bf16", "shared_prefix_bf16"])
@@ -587,6 +630,22 @@ FP8_DECODE_CASES = [
     (16, 2, 8, [1025, 64], (0x00, 0x7F)),
     (12, 3, 16, [700, 33, 1, 1200], (0x30, 0x60)),  # odd kv-head count: one kv head per item
 ]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (32, 2, 128)])
+def test_fp8_decode_refuses_shapes_it_does_not_build(Hq, Hkv, D):
+    """Head size 64 and 16 query heads per kv head have no e4m3 kernel: the call returns PA_ERR_UNSUPPORTED (no
+    launch, no silent fallback) although the same shapes over bf16 pools are served."""
+    N, B, P = 2, 16, 8
+    q = torch.zeros(N, Hq, D, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(P, B, Hkv, D, dtype=torch.uint8, device="cuda")
+    bt = torch.arange(N * 2, dtype=torch.int32, device="cuda").view(N, 2)
+    ctx = torch.tensor([5, 20], dtype=torch.int32, device="cuda")
+    ws = pa.new_decode_workspace(N, Hq, Hkv, D, B, 20)
+    with pytest.raises(pa.PaError) as ei:
+        pa.pa_decode_fp8(q, kc, kc.clone(), bt, ctx, 20, 0.1, 1.0, 1.0, ws)
+    assert ei.value.status == pa.PA_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("case", range(len(FP8_DECODE_CASES)))
