@@ -83,6 +83,14 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 #define PA_PREFILL_EXP2_PAIRS 1
 #endif
 
+// A 32-byte global store (8 words; the address 32-byte aligned): an output row leaves the epilogue in whole
+// 32-byte sectors, half the store instructions of 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // the eight softmax warps (256 threads) only
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
@@ -400,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col0 = half * 64;
         const uint32_t t_own = tmem + lane_off + (half ? kTmemOb : kTmemOa);  // this half's O, row r
         const float sl2 = p.scale_log2;
+        const bool out_al32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         int gt = 0;  // key tiles taken so far
         for (int c = 0; c * (int)gridDim.x < num_items; ++c) {
             const int k = item_of(c);
@@ -600,21 +609,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 16; ++i) t[i] = 0.f;
                 }
                 if (!row_ok) continue;
+                // (the workspace partials are 256-byte aligned; the output takes 32-byte stores when its base
+                // allows, 16-byte ones otherwise)
                 if (prefix_mode) {
-                    float4* po = reinterpret_cast<float4*>(p.part_o + slot * kD + col0 + q4 * 16);
+                    float* po = p.part_o + slot * kD + col0 + q4 * 16;
                     const float f = same ? 1.f : 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        po[i / 4] = make_float4(t[i] * f, t[i + 1] * f, t[i + 2] * f, t[i + 3] * f);
-                } else {
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        uint32_t w8[8];
 #pragma unroll
-                    for (int i = 0; i < 16; i += 8) {
-                        uint4 pk;
-                        pk.x = pack_bf16x2(t[i], t[i + 1]);
-                        pk.y = pack_bf16x2(t[i + 2], t[i + 3]);
-                        pk.z = pack_bf16x2(t[i + 4], t[i + 5]);
-                        pk.w = pack_bf16x2(t[i + 6], t[i + 7]);
-                        *reinterpret_cast<uint4*>(out + q4 * 16 + i) = pk;
+                        for (int i = 0; i < 8; ++i) w8[i] = __float_as_uint(t[h8 * 8 + i] * f);
+                        st_global_v8(po + h8 * 8, w8);
+                    }
+                } else {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(t[2 * i], t[2 * i + 1]);
+                    if (out_al32) {
+                        st_global_v8(out + q4 * 16, pk);
+                    } else {
+                        uint4* o4 = reinterpret_cast<uint4*>(out + q4 * 16);
+                        o4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        o4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
                 }
             }
