@@ -187,8 +187,11 @@ PA_API int pa_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int h
  * hold pa_decode_workspace_size(...) bytes, be 256-byte aligned, and be zeroed
  * once before its first use; the library leaves it zeroed-for-reuse after
  * every call.  One workspace must not serve two calls that may overlap on the
- * GPU.  Supported: head_dim 64 or 128, block_size 8..128 dividing 64 or a
- * multiple of 64, num_q_heads/num_kv_heads in 1..16.
+ * GPU.  Supported: head_dim 64 or 128, block_size 1..1024,
+ * num_q_heads/num_kv_heads in 1..16 (other shapes: PA_ERR_UNSUPPORTED).
+ * bf16 pools with block_size 8, 16, 32 or 64 and up to 8 query heads per kv
+ * head run on the tensor-core kernel; every other supported shape, and fp32,
+ * runs on the CUDA-core kernel.
  */
 PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
               int dtype, const void* k_cache, const void* v_cache, int num_blocks, int block_size,
@@ -280,9 +283,12 @@ PA_API int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_hea
  * Some callers cannot call cudaMalloc where decode runs (a runtime that
  * forbids allocation after start-up, a plugin living inside another
  * framework's memory budget, or a caller that must not trigger the implicit
- * synchronisation an allocation can cause).  This entry point computes
- * exactly what pa_decode computes, with the same arguments minus the
- * workspace: its split-KV scratch is a fixed 16 MiB array in device global
+ * synchronisation an allocation can cause).  This entry point computes the
+ * same attention as pa_decode, with the same arguments minus the workspace,
+ * within the same tolerances (bitwise equal to pa_decode whenever the split
+ * plan is unchanged; where the plan below makes partitions longer, the
+ * partials are rounded and merged differently in the last bits).  Its
+ * split-KV scratch is a fixed 16 MiB array in device global
  * memory owned by the library, which every GPU that loads the library keeps
  * until the process exits.  It allocates nothing (no cudaMalloc / cudaFree,
  * no allocating library routine).
@@ -291,8 +297,11 @@ PA_API int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_hea
  *    single partition are rejected with PA_ERR_WORKSPACE before anything is
  *    launched.
  *  - The first call on a device looks up the array's device address on that
- *    device (cudaGetSymbolAddress) and caches it; make that first call before
- *    any stream capture on the device.
+ *    device (cudaGetSymbolAddress) and caches it for the life of the process;
+ *    make that first call before any stream capture on the device.  A device
+ *    reset (cudaDeviceReset, or a reset of the primary context) invalidates
+ *    the cached address: do not call this entry point on that device after
+ *    one.
  *  - The array is shared by every call and keeps the last call's contents;
  *    each call clears its work-queue counters (an asynchronous memset on
  *    `stream`) before launching.  Calls that may overlap on the GPU (other

@@ -55,15 +55,14 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
                                  const int32_t* context_lens, int max_context_len, float scale,
                                  int32_t* error_count, void* stream) {
     if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
-    if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-    if (num_q_heads / num_kv_heads > 16 || (head_dim != 64 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
-    if (block_size < 1 || block_size > 1024) return PA_ERR_UNSUPPORTED;
+    int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);  // the shapes pa_decode takes
+    if (rc != PA_OK) return rc;
     if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
         return PA_ERR_INVALID_ARG;
     int num_sms = 0;
-    int rc = check_device(&num_sms);
+    rc = check_device(&num_sms);
     if (rc != PA_OK) return rc;
     DecodePlan plan =
         plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, kNoAllocScratchBytes);

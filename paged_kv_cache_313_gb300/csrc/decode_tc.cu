@@ -56,6 +56,8 @@
 //    other stages of the ring meanwhile.
 // Every mbarrier wait is bounded; a timeout counts an error and the kernel
 // still terminates.  The work counter is reset by the last CTA to finish.
+#include <atomic>
+
 #include "decode_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -841,7 +843,10 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     // C::kCtasPerSm CTAs per SM (or as many as are resident at once, should fewer fit), never more
     // CTAs than the largest possible item count: a persistent CTA that is not resident from the start finds
     // the queue empty when it runs
-    static int resident = 0;
+    // (occupancy depends only on the kernel and its launch shape, the same on every GB300; the cached value is
+    // atomic so that concurrent first calls from several host threads are safe)
+    static std::atomic<int> resident_cache{0};
+    int resident = resident_cache.load(std::memory_order_relaxed);
     if (resident == 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8, kPair>, C::kThreads,
@@ -849,6 +854,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
             return check_launch();
         if (n < 1) return PA_ERR_UNSUPPORTED;
         resident = n < C::kCtasPerSm ? n : C::kCtasPerSm;
+        resident_cache.store(resident, std::memory_order_relaxed);
     }
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * resident;

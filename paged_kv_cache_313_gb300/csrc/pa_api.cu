@@ -250,13 +250,19 @@ int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int block_size,
                               num_valid, num_copies, error_count, static_cast<cudaStream_t>(stream));
 }
 
-static int decode_shape_ok(int num_q_heads, int num_kv_heads, int head_dim, int block_size) {
+}  // extern "C"
+
+namespace pa {
+int decode_shape_ok(int num_q_heads, int num_kv_heads, int head_dim, int block_size) {
     if (num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (num_q_heads / num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (block_size < 1 || block_size > 1024) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
+}  // namespace pa
+
+extern "C" {
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                 int max_context_len) {

@@ -50,6 +50,10 @@ int launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 
 inline int elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
+// Shapes pa_decode takes: PA_OK, PA_ERR_INVALID_ARG (head counts that do not
+// group) or PA_ERR_UNSUPPORTED (head_dim, block_size or group out of range).
+int decode_shape_ok(int num_q_heads, int num_kv_heads, int head_dim, int block_size);
+
 // Split-KV partition policy shared by pa_decode and pa_decode_workspace_size.
 struct DecodePlan {
     int partition;   // tokens per split (multiple of 64)

@@ -178,14 +178,16 @@ def test_empty_and_single_token_contexts():
     q = rng.standard_normal((3, Hq, D), dtype=np.float32)
     bt = np.array([[4, -1], [-1, -1], [2, 6]], np.int32)
     ctx = np.array([1, 0, 17], np.int32)
-    want = oracle.decode(q, kc, vc, bt, ctx, 0.1)
     for dt in (torch.float32, torch.bfloat16):
         t = lambda x: torch.from_numpy(x).to(dt).cuda()  # noqa: E731
-        got = _decode_direct(t(q), t(kc), t(vc), torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), 17, 0.1)
+        qd, kd, vd = t(q), t(kc), t(vc)
+        # the oracle reads the same stored values (bf16 bit patterns for bf16)
+        want = oracle.decode(storage_numpy(qd), storage_numpy(kd), storage_numpy(vd), bt, ctx, 0.1)
+        got = _decode_direct(qd, kd, vd, torch.from_numpy(bt).cuda(), torch.from_numpy(ctx).cuda(), 17, 0.1)
         assert torch.all(got[1] == 0)
-        if dt == torch.float32:
-            assert _maxabs(got, want) <= 1e-5
-            assert torch.equal(got[0].cpu(), torch.from_numpy(vc[4, 0]).repeat_interleave(4, 0))
+        assert _maxabs(got, want) <= TOL[dt]
+        # one token: the output is that token's V row exactly (bf16 V rows are representable in bf16)
+        assert torch.equal(got[0].cpu(), vd[4, 0].cpu().repeat_interleave(4, 0))
 
 
 def test_invalid_table_entries_are_skipped_and_counted():
@@ -253,6 +255,13 @@ DECODE_SHAPE_CASES = [
     (16, 2, 128, 8, [1025, 64], torch.bfloat16),
     (128, 8, 128, 16, [300, 1], torch.bfloat16),
     (8, 2, 128, 16, [9000, 33], torch.float32),
+    # block sizes only the CUDA-core kernel takes (1, 48, 128 on bf16 pools; 256 and 1024 on fp32 pools), with
+    # contexts one short of, at and one past a block boundary
+    (8, 2, 128, 1, [1, 300, 1100], torch.bfloat16),
+    (32, 8, 128, 48, [47, 48, 49, 2000], torch.bfloat16),
+    (16, 4, 64, 128, [127, 129, 1300], torch.bfloat16),
+    (8, 8, 128, 256, [255, 257, 1024], torch.float32),
+    (4, 2, 64, 1024, [1023, 1025, 3000], torch.float32),
 ]
 
 

@@ -394,3 +394,122 @@ def test_fp8_write_round_trips_representable_values():
     assert oracle.write_kv_fp8(knew, knew, kc, vc, np.array([0]), scale, scale) == 0
     assert np.array_equal(kc.reshape(-1), codes)
     assert np.array_equal(oracle.dequant_e4m3(kc, scale).reshape(-1), vals.astype(np.float64))
+
+
+def test_fp8_write_reciprocal_rounding_at_non_power_of_two_scales():
+    """The quantising write's reading: code = e4m3(x * (1/scale)) with the reciprocal and the product each
+    rounded to float ("KV cache 显存管理…", KV size formula leaves the element format open; the reading is the
+    one stated for the fp8 pools).  Each case below is a bf16 value whose float product lands exactly on the
+    midpoint between two codes, or just off it, while a plausible slip lands on the other side:
+
+    * scale 0.37f: 1/0.37f rounds to 2.702702760696411 (0x402CF915); 0.2890625 * that = 0.78125000168 in exact
+      arithmetic, which rounds in float to 0.78125, the midpoint of 0.75 (0x34) and 0.8125 (0x35): the tie goes
+      to the even code 0x34.  Keeping the product in double would give 0x35.
+    * scale 0.7f: 1/0.7f = 1.4285714626312256; 0.2734375 * that rounds to 0.390625, the midpoint of 0.375 (0x2C)
+      and 0.40625 (0x2D): 0x2C.  Dividing by the scale in double (0.39062500665) would give 0x2D.
+    * scale 0.9f: 1/0.9f = 1.1111111640930176; 0.3515625 * that rounds to 0.39062503 (above the same midpoint):
+      0x2D.  Dividing by the scale in float gives exactly 0.390625, hence 0x2C.
+    * scale 0.6f: 1/0.6f = 1.6666666269302368; 0.0087890625 * that rounds to 0.0146484375, the midpoint of the
+      largest subnormal 7 * 2^-9 (0x07) and the smallest normal 2^-6 (0x08): the even code 0x08.  Division in
+      double or float, or the product in double, all fall below the midpoint: 0x07.
+    Negated inputs give the same codes with the sign bit set."""
+    import torch
+    cases = [(0.37, 0.2890625, 0x34), (0.7, 0.2734375, 0x2C), (0.9, 0.3515625, 0x2D), (0.6, 0.0087890625, 0x08)]
+    for scale, x, code in cases:
+        vals = torch.tensor([x, -x], dtype=torch.float32)
+        bits = vals.to(torch.bfloat16)
+        assert torch.equal(bits.float(), vals)  # the inputs are exact bf16 values
+        knew = bits.view(torch.int16).numpy().view(np.uint16).reshape(1, 1, 2)
+        vnew = np.zeros_like(knew)
+        kc = np.zeros((1, 1, 1, 2), np.uint8)
+        vc = np.zeros_like(kc)
+        assert oracle.write_kv_fp8(knew, vnew, kc, vc, np.array([0]), scale, 1.0) == 0
+        assert kc.reshape(-1).tolist() == [code, code | 0x80], (scale, x, kc.reshape(-1).tolist())
+        # the same value through the V pool's scale
+        kc[:] = 0
+        vc[:] = 0
+        assert oracle.write_kv_fp8(vnew, knew, kc, vc, np.array([0]), 1.0, scale) == 0
+        assert vc.reshape(-1).tolist() == [code, code | 0x80]
+
+
+# ---- sharing ("什么是 PagedAttention？", 共享但不污染状态): sequences that map the same physical prefix blocks
+
+def _shared_batch(seed, B=16, Hq=8, Hkv=2, D=32):
+    """Four sequences over one pool.  Sequences 0 and 1 share physical prefix blocks 5, 9, 2 and each has a
+    private tail block (7 and 11); block 11 is filled with a copy of block 7, so their K/V are equal token by
+    token.  Sequence 2 shares the prefix but its tail block 13 holds different values.  Sequence 3 holds the
+    same K/V as sequence 0 in entirely different physical blocks (a copy of the prefix in 20, 21, 22 and of the
+    tail in 23)."""
+    rng = np.random.default_rng(seed)
+    P = 24
+    kc = rng.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    vc = rng.standard_normal((P, B, Hkv, D)).astype(np.float32)
+    for dst, src in ((11, 7), (20, 5), (21, 9), (22, 2), (23, 7)):
+        kc[dst] = kc[src]
+        vc[dst] = vc[src]
+    bt = np.array([[5, 9, 2, 7], [5, 9, 2, 11], [5, 9, 2, 13], [20, 21, 22, 23]], np.int32)
+    L = 3 * B + 5
+    ctx = np.full(4, L, np.int32)
+    q1 = rng.standard_normal((Hq, D)).astype(np.float32)
+    q = np.stack([q1, q1, q1, q1])
+    return q, kc, vc, bt, ctx
+
+
+def test_shared_prefix_sequences_give_identical_outputs():
+    """Two sequences of one batch whose tables map the same physical prefix blocks, with equal tails and
+    equal queries, give bitwise-equal outputs; a sequence with the same prefix but a different tail does not;
+    the same K/V at another placement gives the same outputs (paged == contiguous)."""
+    q, kc, vc, bt, ctx = _shared_batch(5)
+    for threads in (1, 4):
+        o = oracle.decode(q, kc, vc, bt, ctx, 0.2, num_threads=threads)
+        assert np.array_equal(o[0], o[1])
+        assert np.array_equal(o[0], o[3])
+        assert not np.allclose(o[0], o[2], atol=1e-6)
+    # with the queries of sequence 1 changed the outputs differ (the rows are not read from one sequence)
+    q2 = q.copy()
+    q2[1] = -q2[1]
+    o2 = oracle.decode(q2, kc, vc, bt, ctx, 0.2)
+    assert np.array_equal(o2[0], o[0]) and not np.allclose(o2[1], o2[0], atol=1e-6)
+    # a shorter context on sequence 1 that stops inside the shared prefix reads only shared blocks: it equals
+    # the same length on sequence 2, whose different tail is then never read
+    ctx2 = ctx.copy()
+    ctx2[1] = ctx2[2] = 2 * kc.shape[1] + 3
+    o3 = oracle.decode(q, kc, vc, bt, ctx2, 0.2)
+    assert np.array_equal(o3[1], o3[2])
+
+
+def test_shared_prefix_prefill_identical_for_identical_chunks():
+    """The same sharing for prefill chunks: chunks of two sequences that share their prefix blocks and have
+    equal tails, with equal queries at equal positions, give bitwise-equal outputs."""
+    q, kc, vc, bt, ctx = _shared_batch(6)
+    n = 9
+    rng = np.random.default_rng(7)
+    qc = rng.standard_normal((n, q.shape[1], q.shape[2])).astype(np.float32)
+    qp = np.concatenate([qc, qc, qc])
+    cu = np.array([0, n, 2 * n, 3 * n], np.int32)
+    start = np.full(3, int(ctx[0]) - n, np.int32)
+    o = oracle.prefill(qp, cu, start, np.array([0, 1, 2], np.int32), kc, vc, bt, ctx, 0.2)
+    assert np.array_equal(o[:n], o[n:2 * n])
+    assert not np.allclose(o[:n], o[2 * n:], atol=1e-6)
+
+
+# ---- the float64 input branch (used for e4m3 pools read back as code * scale)
+
+def test_float64_inputs_equal_the_same_values_as_float32():
+    """Decode and prefill on float64 arrays holding float32 values give exactly the float32 results: the
+    widening is exact and the arithmetic is fp64 either way.  Guards the float64 element loads and sizes."""
+    q, cu, qs, soc, kc, vc, bt, ctx = _prefill_case(seed=3)
+    o32 = oracle.prefill(q, cu, qs, soc, kc, vc, bt, ctx, 0.35)
+    o64 = oracle.prefill(q.astype(np.float64), cu, qs, soc, kc.astype(np.float64), vc.astype(np.float64), bt, ctx,
+                         0.35)
+    assert np.array_equal(o32, o64)
+    qd = q[:2]
+    d32 = oracle.decode(qd, kc, vc, bt, ctx, 0.35)
+    d64 = oracle.decode(qd.astype(np.float64), kc.astype(np.float64), vc.astype(np.float64), bt, ctx, 0.35)
+    assert np.array_equal(d32, d64)
+    # values that float32 cannot hold are used as they are: a float64 pool with a 1e-12 offset on one key
+    # changes the scores (a float32 load of the same memory would not see it)
+    kc64 = kc.astype(np.float64)
+    kc64[bt[0, 0], 0, 0, 0] += 1e-12 * 2 ** 20
+    d64b = oracle.decode(qd.astype(np.float64), kc64, vc.astype(np.float64), bt, ctx, 0.35)
+    assert not np.array_equal(d64b[0], d32[0])
