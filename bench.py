@@ -45,6 +45,8 @@ DEFAULT_WORKLOAD = "decode_bf16"
 FLUSH_BYTES = 512 << 20
 # workloads whose oracle is also timed on one thread (the small correctness case and the default decode batch)
 SINGLE_THREAD_ORACLE = ("tiny_fp32", "decode_bf16")
+# the configurations measured after the headline (each at --sweep-steps), reported under "workloads"
+SWEEP = ("tiny_fp32", "decode_bf16", "longctx_bf16", "shared_prefix_bf16", "mixed_bf16", "decode_fp8")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -66,6 +68,13 @@ def parse_args():
                     help="plain paged decode even where decode sequences share prefixes")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch the timed steps eagerly instead of replaying a captured CUDA graph")
+    ap.add_argument("--sustained-seconds", type=float, default=1.5,
+                    help="after the K timed steps, flushed steps back to back for this long (clock samples)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="measure only the headline workload (default: also every other configuration)")
+    ap.add_argument("--sweep-steps", type=int, default=20, help="timed steps per configuration of the sweep")
+    ap.add_argument("--sweep-cpu-seconds", type=float, default=4.0,
+                    help="target CPU time of each sweep configuration's oracle sample (at least one full step)")
     return ap.parse_args()
 
 
@@ -282,7 +291,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.l2_flush),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n} full oracle steps of workload {w.name} (fp64 C, {threads} threads)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -312,6 +321,198 @@ def workload_config(w, l2_flush: str = "write"):
 
 
 # ------------------------------------------------------------- native arm
+def launches_per_step(step, w, pa):
+    """Our kernels per step: the fused slot mapping + KV write (unless the decode kernel writes every new token
+    itself), the decode kernel(s) and the split-KV merge, and the prefill kernel."""
+    decode_launches = 0
+    if step.use_cascade:  # decode (prefix items + tails) and merge; a separate prefix pass for groups over 32 rows
+        decode_launches = 2 if w.max_group_size * (w.num_q_heads // w.num_kv_heads) <= 32 else 3
+    elif w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
+        _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                      step.max_context_len)
+        decode_launches = 1 + (1 if splits > 1 else 0)
+    write_launches = 0 if step.fused_decode_write and not w.num_chunks else 1
+    return write_launches + decode_launches + (1 if w.num_chunks else 0)
+
+
+def decode_kernel_name(step, w):
+    if step.use_cascade:
+        return "pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; decode_merge_kernel)"
+    if w.kv_fp8:
+        return "pa_decode_fp8 (decode_tc_kernel over e4m3 pools + decode_merge_kernel)"
+    if step.fused_decode_write:
+        return "pa_decode_write (decode_tc_kernel with the decode tokens' KV write + decode_merge_kernel)"
+    if w.dtype.is_floating_point and w.elem_bytes == 4:
+        return "pa_decode (decode_fma_kernel, fp32 + decode_merge_kernel)"
+    return "pa_decode (decode_tc_kernel + decode_merge_kernel)"
+
+
+class Flusher:
+    """Evicts the step's data from L2 between timed steps (outside the events): a 512 MiB write, then
+    (write-read) a 512 MiB read of another buffer, so that the flush's dirty lines are written back before
+    the next timed step and not inside it."""
+
+    def __init__(self, torch, dev, mode):
+        self.buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        other = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev) if mode == "write-read" else None
+        self.other = other.view(torch.int64) if other is not None else None
+
+    def __call__(self, v):
+        self.buf.fill_(v)
+        if self.other is not None:
+            self.other.sum()  # a plain read of the 512 MiB (no widening copy)
+
+
+def measure(w, args, dev, flush, K, graph=True, sustained_s=0.0, sampler=None, barrier=None):
+    """Time one workload's step on the device: K flushed steps (graph replays), the decode call and the prefill
+    call alone (eager, flushed) for the roofline, K steps with a warm L2, the step end to end from pinned host
+    memory, and optionally a sustained leg of back-to-back flushed steps lasting `sustained_s` seconds.
+    Returns a dict of results (per rank; the caller takes the max over ranks)."""
+    import torch
+
+    from paged_kv_cache_313_gb300 import pa
+    from paged_kv_cache_313_gb300.runner import DeviceStep
+
+    step = DeviceStep(w, dev, cascade=args.cascade)
+    stream = torch.cuda.current_stream(dev)
+    sync = barrier or (lambda: torch.cuda.synchronize(dev))
+    for _ in range(max(3, args.warmup)):
+        flush(1)
+        step.run()
+    sync()
+    if graph:
+        step.capture()
+        for _ in range(3):
+            flush(1)
+            step.replay()
+        sync()
+
+    def timed_steps(n, flush_each=True):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            if flush_each:
+                flush(i & 0xFF)
+            ev[i][0].record(stream)
+            if graph:
+                step.replay()
+            else:
+                step.run()
+            ev[i][1].record(stream)
+        return ev
+
+    # ---- timed region: exactly K whole steps, L2 flushed before each (outside the events)
+    sync()
+    t0 = time.time()
+    ev = timed_steps(K)
+    sync()
+    t1 = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- per-kernel times (eager launches, same flush) for the roofline
+    K1 = max(3, min(K, 100))
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K1)]
+    for i in range(K1):
+        e = kev[i]
+        flush(i & 0xFF)
+        e[0].record(stream)
+        step.write_stage()
+        e[1].record(stream)
+        step.decode_stage()
+        e[2].record(stream)
+        step.prefill()
+        e[3].record(stream)
+    sync()
+    write_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    decode_ms = [e[1].elapsed_time(e[2]) for e in kev]
+    prefill_ms = [e[2].elapsed_time(e[3]) for e in kev]
+
+    # ---- the same K steps back to back with no L2 flush between them (context for the flushed number)
+    wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush(0)
+    wa.record(stream)
+    for _ in range(K):
+        if graph:
+            step.replay()
+        else:
+            step.run()
+    wb.record(stream)
+    sync()
+    warm_ms = wa.elapsed_time(wb) / K
+
+    # ---- sustained: flushed steps back to back for at least sustained_s seconds, so that clock samples
+    # (every 100 ms) fall inside the measured work
+    sustained = None
+    if sustained_s > 0:
+        per = statistics.mean(step_ms) + 0.2  # the flush between steps takes about 0.2 ms
+        n = max(K, int(sustained_s * 1e3 / per) + 1)
+        sync()
+        s0 = time.time()
+        sev = timed_steps(n)
+        sync()
+        s1 = time.time()
+        sms = [a.elapsed_time(b) for a, b in sev]
+        sustained = {"steps": n, "ms_per_step": statistics.mean(sms), "wall_s": s1 - s0,
+                     "clocks": sampler.summary(s0, s1) if sampler else None}
+
+    # ---- end to end through the public API: the packed inputs copied in from pinned host memory (one
+    # copy), then the step, whose kernels store the outputs into a pinned host buffer (d2h: those bytes)
+    host_in = step.pinned_inputs()
+    host_out = step.pinned_outputs()
+    step.step_from_host(host_in, host_out)
+    if graph:
+        step.capture_from_host(host_in, host_out)
+    sync()
+    e2e_ms = []
+    K2 = max(1, min(K, 50))
+    for i in range(K2):
+        flush(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step.run_from_host(host_in, host_out, graph=graph)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    errors = step.errors()
+    res = {"step": step, "step_ms": step_ms, "decode_ms": decode_ms, "write_ms": write_ms,
+           "prefill_ms": prefill_ms, "warm_ms": warm_ms, "e2e_ms": e2e_ms, "K2": K2, "t0": t0, "t1": t1,
+           "h2d": host_in.numel() * host_in.element_size(), "d2h": host_out.numel() * host_out.element_size(),
+           "errors": errors, "sustained": sustained, "launches_per_step": launches_per_step(step, w, pa)}
+    return res
+
+
+def roofline_of(w, step, mean_dec, hbm, peak_kind):
+    alg_bytes = decode_algorithmic_bytes(w)  # each physical K/V slot once
+    if step.fused_decode_write:  # the decode tokens' new K/V rows: read from k_new/v_new, written to the pools
+        alg_bytes += 2 * w.num_decode * w.kv_bytes_per_token()
+    logical_bytes = decode_algorithmic_bytes(w, unique=False)  # every sequence's whole context
+    achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": decode_kernel_name(step, w), "achieved": achieved, "peak": hbm,
+            "unit": "GB/s", "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+            "algorithmic_bytes_per_launch": alg_bytes, "ms_per_launch": mean_dec,
+            "logical_bytes_per_launch": logical_bytes, "effective_gbs": logical_bytes / (mean_dec * 1e-3) / 1e9,
+            "traffic": recorded_traffic("pa_decode", w.name)}
+
+
+def prefill_of(w, prefill_ms, bf16_tf, peak_kind):
+    fl = prefill_flops(w)
+    pm = statistics.mean(prefill_ms)
+    return {"kernel": "prefill_tc_kernel", "bound": "tensor", "flops_per_launch": fl, "ms_per_launch": pm,
+            "achieved_tflops": fl / (pm * 1e-3) / 1e12, "peak_tflops": bf16_tf,
+            "frac": fl / (pm * 1e-3) / 1e12 / bf16_tf, "peak_kind": f"{peak_kind} bf16_tflops (burst)"}
+
+
+def cpu_baseline_of(w, seconds, single_thread=False):
+    per, n, threads = oracle_step_time(w, seconds)
+    out = {"value": w.num_decode / per, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "nproc": os.cpu_count(),
+           "sample": f"{n} full oracle step(s) of workload {w.name} (fp64 C, {threads} threads)"}
+    if single_thread and threads > 1:
+        per1, n1, _ = oracle_step_time(w, min(5.0, seconds), threads=1)
+        out["single_thread"] = {"value": w.num_decode / per1, "unit": "tokens/s", "cores": 1,
+                                "sample": f"{n1} full oracle step(s) of workload {w.name} (fp64 C, 1 thread)"}
+    return out
+
+
 def run_native(args):
     import torch
 
@@ -324,137 +525,36 @@ def run_native(args):
 
     from paged_kv_cache_313_gb300 import pa, sharding
     from paged_kv_cache_313_gb300 import workloads as W
-    from paged_kv_cache_313_gb300.runner import DeviceStep
 
     pa.lib()  # fail loudly if the CUDA library is missing
-    w = W.make(args.workload, sharding.shard_seed(args.seed, rank))
-    step = DeviceStep(w, dev, cascade=args.cascade)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    other = torch.ones(FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.l2_flush == "write-read" else None
-
-    def flush_l2(v):
-        """Evict the step's data from L2 (outside the timed events): a 512 MiB write, then (write-read)
-        a 512 MiB read of another buffer, so that the flush's dirty lines are written back here and
-        not inside the next timed step."""
-        flush.fill_(v)
-        if other is not None:
-            other.view(torch.int64).sum()  # a plain read of the 512 MiB (no widening copy)
-    decode_launches = 0
-    if step.use_cascade:  # decode (prefix items + tails) and merge; a separate prefix pass for groups over 32 rows
-        decode_launches = 2 if w.max_group_size * (w.num_q_heads // w.num_kv_heads) <= 32 else 3
-    elif w.num_decode:  # the decode kernel, plus the split-KV merge kernel when contexts span partitions
-        _, splits = pa.pa_decode_plan(w.num_decode, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
-                                      step.max_context_len)
-        decode_launches = 1 + (1 if splits > 1 else 0)
-    write_launches = 0 if step.fused_decode_write and not w.num_chunks else 1  # slot mapping + KV write
-    launches_per_step = write_launches + decode_launches + (1 if w.num_chunks else 0)
+    flush = Flusher(torch, dev, args.l2_flush)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(max(3, args.warmup)):
-        flush_l2(1)
-        step.run()
-    barrier()
-    if args.graph:
-        step.capture()
-        for _ in range(3):
-            flush_l2(1)
-            step.replay()
-        barrier()
-
-    # ---- timed region: exactly K whole steps, L2 flushed before each (outside the events)
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     visible = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = visible.split(",")[local].strip() if visible else str(local)
     sampler = ClockSampler(smi_index)
     time.sleep(0.3)
-    barrier()
-    t0 = time.time()
-    for i in range(K):
-        flush_l2(i & 0xFF)
-        ev[i][0].record(stream)
-        if args.graph:
-            step.replay()
-        else:
-            step.run()
-        ev[i][1].record(stream)
-    barrier()
-    t1 = time.time()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-
-    # ---- per-kernel times (eager launches, same flush) for the roofline
-    K1 = max(3, min(K, 100))
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K1)]
-    for i in range(K1):
-        e = kev[i]
-        flush_l2(i & 0xFF)
-        e[0].record(stream)
-        step.write_stage()
-        e[1].record(stream)
-        step.decode_stage()
-        e[2].record(stream)
-        step.prefill()
-        e[3].record(stream)
-    barrier()
-    write_ms = [e[0].elapsed_time(e[1]) for e in kev]
-    decode_ms = [e[1].elapsed_time(e[2]) for e in kev]
-    prefill_ms = [e[2].elapsed_time(e[3]) for e in kev]
-
-    # ---- the same K steps back to back with no L2 flush between them (context for the flushed number:
-    # whatever of the step's data is still in the 129 MB L2 is read from there)
-    wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush_l2(0)
-    wa.record(stream)
-    for i in range(K):
-        if args.graph:
-            step.replay()
-        else:
-            step.run()
-    wb.record(stream)
-    barrier()
-    warm_ms = wa.elapsed_time(wb) / K
-
-    # ---- end to end through the public API: the packed inputs copied in from
-    # pinned host memory (one copy), then the step, whose kernels store the
-    # outputs straight into a pinned host buffer (d2h: those output bytes)
-    host_in = step.pinned_inputs()
-    host_out = step.pinned_outputs()
-    step.step_from_host(host_in, host_out)
-    if args.graph:
-        step.capture_from_host(host_in, host_out)
-    barrier()
-    h2d = host_in.numel() * host_in.element_size()
-    d2h = host_out.numel() * host_out.element_size()
-    e2e_ms = []
-    K2 = max(1, min(K, 50))
-    for i in range(K2):
-        flush_l2(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step.run_from_host(host_in, host_out, graph=args.graph)
-        b.record(stream)
-        b.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    sampler.stop()
-    errors = step.errors()
-
-    mean_step, mean_dec, mean_e2e, median_step, warm_step = sharding.max_over_ranks(
-        [statistics.mean(step_ms), statistics.mean(decode_ms), statistics.mean(e2e_ms), statistics.median(step_ms),
-         warm_ms], device=dev)
-
     hbm, bf16_tf, bf16_tf_sus, peak_kind = peaks()
-    alg_bytes = decode_algorithmic_bytes(w)  # each physical K/V slot once
-    if step.fused_decode_write:  # the decode tokens' new K/V rows: read from k_new/v_new, written to the pools
-        alg_bytes += 2 * w.num_decode * w.kv_bytes_per_token()
-    logical_bytes = decode_algorithmic_bytes(w, unique=False)  # every sequence's whole context
-    achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
+
+    # ---- the headline workload: K steps, as the contract times them, then a sustained leg
+    w = W.make(args.workload, sharding.shard_seed(args.seed, rank))
+    K = args.steps
+    r = measure(w, args, dev, flush, K, graph=args.graph, sustained_s=args.sustained_seconds, sampler=sampler,
+                barrier=barrier)
+    step = r["step"]
+    sus = r["sustained"]
+    mean_step, mean_dec, mean_e2e, median_step, warm_step, sus_step = sharding.max_over_ranks(
+        [statistics.mean(r["step_ms"]), statistics.mean(r["decode_ms"]), statistics.mean(r["e2e_ms"]),
+         statistics.median(r["step_ms"]), r["warm_ms"], sus["ms_per_step"] if sus else 0.0], device=dev)
     tokens = sharding.total_units(w.num_decode)
     value = tokens / (mean_step * 1e-3)
+    clocks = (sus or {}).get("clocks") or sampler.summary(r["t0"], r["t1"])
+    if clocks is not None and sus is not None:
+        clocks["window"] = "sustained leg (the headline step, flushed, back to back)"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step, "ms_per_step_median": median_step, "higher_is_better": True, "scaling": "weak",
@@ -464,48 +564,67 @@ def run_native(args):
         "config": workload_config(w, args.l2_flush),
         "kv_read_gbs": (sum(int(x) for x in w.context_lens[: w.num_decode]) * w.kv_bytes_per_token() * world)
                        / (mean_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm",
-                     "kernel": ("pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; "
-                                "decode_merge_kernel)" if step.use_cascade
-                                else "pa_decode_fp8 (decode_tc_kernel over e4m3 pools + decode_merge_kernel)"
-                                if w.kv_fp8
-                                else "pa_decode_write (decode_tc_kernel with the decode tokens' KV write + "
-                                     "decode_merge_kernel)" if step.fused_decode_write
-                                else "pa_decode (decode_tc_kernel + decode_merge_kernel)"),
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_kind": f"{peak_kind} hbm_gbs (copy)",
-                     "algorithmic_bytes_per_launch": alg_bytes, "ms_per_launch": mean_dec,
-                     "logical_bytes_per_launch": logical_bytes,
-                     "effective_gbs": logical_bytes / (mean_dec * 1e-3) / 1e9,
-                     "traffic": recorded_traffic("pa_decode", w.name)},
-        "stage_ms": {"kv_write (separate launch)": statistics.mean(write_ms), "decode": mean_dec,
-                     "prefill": statistics.mean(prefill_ms)},
-        "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e, "steps": K2,
+        "roofline": roofline_of(w, step, mean_dec, hbm, peak_kind),
+        "stage_ms": {"kv_write (separate launch)": statistics.mean(r["write_ms"]), "decode": mean_dec,
+                     "prefill": statistics.mean(r["prefill_ms"])},
+        "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": mean_e2e, "steps": r["K2"],
                 "launch": "cuda_graph" if args.graph else "eager"},
         "warm_l2": {"value": tokens / (warm_step * 1e-3), "unit": "tokens/s", "ms_per_step": warm_step, "steps": K,
                     "note": "the same step repeated with no L2 flush between steps"},
         "step_launch": "cuda_graph" if args.graph else "eager",
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * r["launches_per_step"],
         "kv_memory": kv_memory(w),
-        "clocks": sampler.summary(t0, t1),
-        "device_errors": errors,
+        "clocks": clocks,
+        "device_errors": r["errors"],
     }
+    if sus is not None:
+        line["sustained"] = {"value": tokens / (sus_step * 1e-3), "unit": "tokens/s", "ms_per_step": sus_step,
+                             "steps": sus["steps"], "wall_s": sus["wall_s"], "clocks": sus["clocks"],
+                             "note": "flushed steps back to back for about "
+                                     f"{args.sustained_seconds:g} s; not part of gpu_launches"}
     if w.num_chunks:
-        fl = prefill_flops(w)
-        pm = statistics.mean(prefill_ms)
-        line["prefill"] = {"flops_per_launch": fl, "ms_per_launch": pm, "achieved_tflops": fl / (pm * 1e-3) / 1e12,
-                           "peak_tflops": bf16_tf, "frac": fl / (pm * 1e-3) / 1e12 / bf16_tf}
+        line["prefill"] = prefill_of(w, r["prefill_ms"], bf16_tf, peak_kind)
     if rank == 0 and not args.no_cpu_baseline:
-        per, n, threads = oracle_step_time(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": w.num_decode / per, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "nproc": os.cpu_count(),
-                                "sample": f"{n} full oracle steps of workload {w.name} (fp64 C, {threads} threads)"}
-        if w.name in SINGLE_THREAD_ORACLE and threads > 1:
-            per1, n1, _ = oracle_step_time(w, min(5.0, args.cpu_seconds), threads=1)
-            line["cpu_baseline"]["single_thread"] = {
-                "value": w.num_decode / per1, "unit": "tokens/s", "cores": 1,
-                "sample": f"{n1} full oracle steps of workload {w.name} (fp64 C, 1 thread)"}
+        line["cpu_baseline"] = cpu_baseline_of(w, args.cpu_seconds, single_thread=w.name in SINGLE_THREAD_ORACLE)
+    del step, r
+    torch.cuda.empty_cache()
+
+    # ---- every other configuration of the workload list: the same measurements at fewer steps
+    if args.sweep:
+        per = {}
+        headline_entry = {"value": value, "ms_per_step": mean_step, "roofline_frac": line["roofline"]["frac"],
+                          "e2e": line["e2e"]["value"], "note": "the headline above"}
+        if "cpu_baseline" in line:
+            headline_entry["cpu_baseline"] = line["cpu_baseline"]["value"]
+        for name in SWEEP:
+            if name == w.name:
+                per[name] = headline_entry
+                continue
+            ws = W.make(name, sharding.shard_seed(args.seed, rank))
+            rs = measure(ws, args, dev, flush, args.sweep_steps, graph=args.graph)
+            st = rs["step"]
+            ms, md, me = sharding.max_over_ranks([statistics.mean(rs["step_ms"]), statistics.mean(rs["decode_ms"]),
+                                                  statistics.mean(rs["e2e_ms"])], device=dev)
+            tok = sharding.total_units(ws.num_decode)
+            rf = roofline_of(ws, st, md, hbm, peak_kind)
+            entry = {"value": tok / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": args.sweep_steps,
+                     "config": workload_config(ws, args.l2_flush),
+                     "roofline": {k: rf[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                                     "algorithmic_bytes_per_launch", "ms_per_launch",
+                                                     "logical_bytes_per_launch", "effective_gbs", "traffic")},
+                     "e2e": {"value": tok / (me * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": rs["h2d"],
+                             "d2h_bytes_per_step": rs["d2h"], "ms_per_step": me},
+                     "gpu_launches": args.sweep_steps * rs["launches_per_step"], "device_errors": rs["errors"]}
+            if ws.num_chunks:
+                entry["prefill"] = prefill_of(ws, rs["prefill_ms"], bf16_tf, peak_kind)
+            if rank == 0 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline_of(ws, args.sweep_cpu_seconds)
+            per[name] = entry
+            del st, rs, ws
+            torch.cuda.empty_cache()
+        line["workloads"] = per
+    sampler.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
