@@ -381,6 +381,21 @@ PA_API int pa_copy_blocks(void* k_cache, void* v_cache, int num_blocks, int bloc
                    int head_dim, int dtype, const int32_t* src_blocks, const int32_t* dst_blocks,
                    const int32_t* num_valid, int num_copies, int32_t* error_count, void* stream);
 
+/*
+ * Self-check of the bounded wait that lets every kernel of this library
+ * terminate (no counterpart on the pages: it checks the library's own error
+ * path, without a fault).  Every kernel waits on its mbarriers with a poll
+ * limit; a wait that runs out counts an error in error_count and the kernel
+ * finishes.  This launches one warp that waits, with `polls` polls (1..65536,
+ * each a suspended try-wait of at most about 20 us), on a barrier nothing
+ * arrives on (arrive == 0) or that it arrived on first (arrive != 0).
+ *   result       device int32 [1]: 1 if the wait saw its phase complete, 0 if
+ *                it gave up
+ *   error_count  device int32 [1] or NULL: incremented when the wait gave up
+ * PA_ERR_INVALID_ARG for polls out of range or a NULL result.
+ */
+PA_API int pa_check_bounded_wait(int polls, int arrive, int32_t* result, int32_t* error_count, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

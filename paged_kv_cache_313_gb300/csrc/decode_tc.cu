@@ -54,8 +54,13 @@
 //    partition) or a partial for the split-KV merge kernel (decode_merge.cu);
 //    no fence, ticket or wait on other CTAs.  The producer keeps filling the
 //    other stages of the ring meanwhile.
-// Every mbarrier wait is bounded; a timeout counts an error and the kernel
-// still terminates.  The work counter is reset by the last CTA to finish.
+// Every wait is bounded, the consumers' epilogue barrier included (an
+// mbarrier, not a named barrier, so a warp that gave up cannot strand the
+// others); a timeout counts an error and the kernel still terminates.  Before
+// a CTA exits, its producer waits (bounded) for the last phase it armed on
+// every ring slot, so no bulk copy it issued is still landing in shared
+// memory when the CTA is gone.  The work counter is reset by the last CTA to
+// finish.
 #include <atomic>
 
 #include "decode_common.cuh"
@@ -139,7 +144,8 @@ struct TcCfg {
     static constexpr int kScan = kRed + kRedBytes;
     static constexpr int kInfo = kScan + 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
-    static constexpr int kCtx = kBars + 2 * kStages * 8;
+    // full[kStages], empty[kStages], and the consumers' epilogue barrier
+    static constexpr int kCtx = kBars + (2 * kStages + 1) * 8;
     // an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA, and 1 KiB of each CTA's
     // allocation goes to aligning the base; every array lives in the dynamic allocation
     static constexpr int kSmemCap = 228 * 1024 / kCtasPerSm - 2 * 1024;
@@ -162,10 +168,6 @@ struct TileRows {
     __device__ __forceinline__ uint32_t at(uint32_t r, uint32_t half, uint32_t chunk) const {
         return row(r) + half * half_stride + ((chunk ^ (r & 7u)) << 4);
     }
-};
-
-struct ConsumerBarrier {
-    __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 };
 
 // Item -> (sequence, partition, kv head) through the prefix sum cum[0..N] of
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + C::kInfo);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBars);
     uint64_t* empty = full + C::kStages;
+    uint64_t* cons_bar = empty + C::kStages;  // the consumer warps' epilogue barrier (bounded)
     auto red_m = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed);
     auto red_l = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed + C::kRedBytes / 2);
     int* warp_tot = reinterpret_cast<int*>(smem + C::kScan);
@@ -235,6 +238,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 mbar_init(&full[i], 1);
                 mbar_init(&empty[i], C::kConsumerWarps);
             }
+            mbar_init(cons_bar, C::kConsumerWarps);
             fence_mbar_init();
         }
         __syncthreads();
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     if (skip > 0) lvalid &= skip >= 64 ? 0ull : ~((1ull << skip) - 1ull);
                 }
                 if (stage_no >= (uint32_t)C::kStages &&
-                    !mbar_wait(&empty[slot], ((stage_no / C::kStages) - 1) & 1)) {
+                    !mbar_wait_warp(&empty[slot], ((stage_no / C::kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -453,18 +457,28 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             d = d2;
             raw = raw2;
         }
-        // terminator stage
+        // terminator stage: armed only once its slot is free (the consumers released the slot, so the
+        // slot's previous phase of `full` has completed and a new arrival starts the next phase)
+        uint32_t armed = stage_no;  // phases of `full` armed so far, in ring order
         {
             const int slot = stage_no % C::kStages;
             const bool free_slot =
-                stage_no < (uint32_t)C::kStages || mbar_wait(&empty[slot], ((stage_no / C::kStages) - 1) & 1);
+                stage_no < (uint32_t)C::kStages || mbar_wait_warp(&empty[slot], ((stage_no / C::kStages) - 1) & 1);
             if (lane == 0) {
                 if (!ok || !free_slot) count_error(p.error_count);
-                info[slot].s = -1;
-                info[slot].flags = 0;
-                mbar_arrive_expect_tx(&full[slot], 0);
+                if (free_slot) {
+                    info[slot].s = -1;
+                    info[slot].flags = 0;
+                    mbar_arrive_expect_tx(&full[slot], 0);
+                }
             }
+            if (free_slot) ++armed;
         }
+        // drain: every copy this CTA issued has landed before it exits.  On the normal path the consumers
+        // have waited for every armed phase already and this returns at once; after a timeout it keeps
+        // the CTA (and its shared memory) alive until the copies in flight complete.
+        if (lane == 0 && !drain_ring(full, C::kStages, armed)) count_error(p.error_count);
+        __syncwarp();
     } else {
         // ================================================================ consumers
         const int g4 = lane >> 2, c4 = lane & 3;
@@ -484,10 +498,13 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
         // base-2 score scale: fp8 pools fold the softmax scale into the f16 queries and the K scale here
         const float sl2 = kFp8 ? p.k_scale : p.scale_log2;
         int item_parity = 0;
+        // the item epilogue's barrier among the four consumer warps: an mbarrier with a bounded wait, so a
+        // consumer warp that gave up on a stage can never leave the others blocked in an epilogue
+        BoundedWarpBarrier cbar{cons_bar, 0u};
         const TileRows tr{(uint32_t)B * 128u, (uint32_t)(C::kSegs * B * 128), __ffs(B) - 1};
         for (uint32_t stage_no = 0;; ++stage_no) {
             const int slot = stage_no % C::kStages;
-            if (!mbar_wait(&full[slot], (stage_no / C::kStages) & 1)) {
+            if (!mbar_wait_warp(&full[slot], (stage_no / C::kStages) & 1)) {
                 if (lane == 0) count_error(p.error_count);
                 break;
             }
@@ -731,7 +748,6 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             // back to the producer only after that.  The (m, l) exchange
             // arrays alternate between items so that a warp running ahead
             // into the next epilogue never overwrites values still being read.
-            const ConsumerBarrier bar;
             const int par = item_parity;
             item_parity ^= 1;
             float L0 = l0, L1 = l1;
@@ -746,7 +762,10 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 red_l[par][warp][2 * c4] = L0;
                 red_l[par][warp][2 * c4 + 1] = L1;
             }
-            bar();  // every warp is done with this stage's K/V, and the states are visible
+            if (!cbar.sync()) {  // every warp is done with this stage's K/V, and the states are visible
+                if (lane == 0) count_error(p.error_count);
+                break;
+            }
             float M0 = -INFINITY, M1 = -INFINITY;  // over the warps that share this warp's kv head
 #pragma unroll
             for (int w = hp * C::kWarpsPerHead; w < (hp + 1) * C::kWarpsPerHead; ++w) {
@@ -770,7 +789,10 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 }
             }
             fence_proxy_async_smem();  // these writes precede the slot's next TMA write
-            bar();
+            if (!cbar.sync()) {
+                if (lane == 0) count_error(p.error_count);
+                break;
+            }
             // the item's query rows (G per kv head, the heads' rows adjacent in q and out)
             __nv_bfloat16* out =
                 static_cast<__nv_bfloat16*>(p.out) + ((size_t)inf.s * p.num_q_heads + (size_t)inf.kvh * G) * D;

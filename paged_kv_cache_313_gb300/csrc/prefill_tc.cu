@@ -39,7 +39,11 @@
 //             bf16 into tensor memory, zero V rows past the last valid key,
 //             and finally normalise O and store the output rows.
 // All waits are bounded (an error is counted and the kernel still finishes);
-// TMEM is always freed.
+// TMEM is always freed.  Before the CTA exits, the producers wait (bounded)
+// for the last phase they armed on each of their barriers and the MMA warp
+// commits once more and waits for that commit, so no bulk copy is landing in
+// shared memory and no MMA is writing tensor memory when the CTA frees its
+// tensor memory and exits.
 #include "pa_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -70,8 +74,8 @@ constexpr int kK = kQ + kTileBytes;
 constexpr int kV = kK + kKStages * kTileBytes;
 constexpr int kBars = kV + kVStages * kTileBytes;
 // barriers: q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2], p_full[2], o_done[2], m_full[8],
-// q_empty, o_free
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + kMaskSlots + 2;
+// q_empty, o_free, mma_drain
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + kMaskSlots + 3;
 constexpr int kMask = kBars + kNumBars * 8;  // uint32 [8][4]: key-validity mask of tile j in slot j%8
 constexpr int kTmemSlot = kMask + kMaskSlots * 4 * 4;
 constexpr size_t kSmemBytes = 1024 + kTmemSlot + 16;
@@ -112,6 +116,8 @@ struct Bars {
     __device__ uint64_t* q_empty() const { return base + 7 + 2 * kKStages + 2 * kVStages + kMaskSlots; }
     // the softmax warps have read O (and left the S buffers) in an item's epilogue
     __device__ uint64_t* o_free() const { return base + 8 + 2 * kKStages + 2 * kVStages + kMaskSlots; }
+    // every tcgen05.mma the MMA warp issued has completed (its last commit, before tensor memory is freed)
+    __device__ uint64_t* mma_drain() const { return base + 9 + 2 * kKStages + 2 * kVStages + kMaskSlots; }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -196,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kMaskSlots; ++i) mbar_init(bars.m_full(i), 1);
         mbar_init(bars.q_empty(), 1);
         mbar_init(bars.o_free(), 8);
+        mbar_init(bars.mma_drain(), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -228,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         int gt = 0, gi = 0;  // key tiles, and items with keys, taken so far
+        uint32_t armed = 0, armed_q = 0;  // phases armed on this producer's ring (K or V) and on q_full
         for (int c = 0; c * (int)gridDim.x < num_items && ok; ++c) {
             const int k = item_of(c);
             Item d;
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nblk = (nkeys + B - 1) / B;
             if (!v_side && nt > 0) {  // with no keys nothing is loaded (nor left in flight)
                 // the Q tile; its buffer is free once the previous item's last QK^T completed
-                if (gi > 0 && !mbar_wait(bars.q_empty(), (gi - 1) & 1)) {
+                if (gi > 0 && !mbar_wait_warp(bars.q_empty(), (gi - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -246,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 2; ++h)
                         tma_load_3d(smem + kQ + h * kHalf, &tmq, h * 64, kvh * G, d.r0 + d.i0, bars.q_full());
                 }
+                ++armed_q;
             }
             int pb_lane = -1;
             uint32_t lbytes = 0, lvm[4] = {0u, 0u, 0u, 0u};
@@ -292,13 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int w = 0; w < 4; ++w) vm[w] = __shfl_sync(0xffffffffu, lvm[w], l);
                     const int st = g % kKStages;
-                    if (g >= kKStages && !mbar_wait(bars.k_empty(st), ((g / kKStages) - 1) & 1)) ok = false;
+                    if (g >= kKStages && !mbar_wait_warp(bars.k_empty(st), ((g / kKStages) - 1) & 1)) ok = false;
                     if (!ok) break;
                     if (lane == 0) {
                         for (int w = 0; w < 4; ++w) vmask[(g % kMaskSlots) * 4 + w] = vm[w];
                         mbar_arrive(bars.m_full(g % kMaskSlots));
                         mbar_arrive_expect_tx(bars.k_full(st), bytes);
                     }
+                    ++armed;
                     __syncwarp();  // armed before any copy is issued
                     if (my_load)
                         tma_load_2d(smem + kK + st * kTileBytes + h * kHalf + blk * B * 128, &tmk, kvh * kD + h * 64,
@@ -306,9 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     // V tile j (its slot is free once PV_{j-kVStages} completed)
                     const int vs = g % kVStages;
-                    if (g >= kVStages && !mbar_wait(bars.v_empty(vs), ((g / kVStages) - 1) & 1)) ok = false;
+                    if (g >= kVStages && !mbar_wait_warp(bars.v_empty(vs), ((g / kVStages) - 1) & 1)) ok = false;
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(bars.v_full(vs), bytes);
+                    ++armed;
                     __syncwarp();
                     if (my_load)
                         tma_load_2d(smem + kV + vs * kTileBytes + h * kHalf + blk * B * 128, &tmv, kvh * kD + h * 64,
@@ -320,6 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nt > 0) ++gi;
         }
         if (!ok && lane == 0) count_error(p.error_count);
+        // drain: every copy this warp issued has landed before the CTA exits (at once on the normal path,
+        // where the MMA warp waited for every armed phase; after a timeout, copies still in flight)
+        if (lane == 0) {
+            const bool drained = v_side ? drain_ring(bars.v_full(0), kVStages, armed)
+                                        : drain_ring(bars.k_full(0), kKStages, armed) &&
+                                              drain_ring(bars.q_full(), 1, armed_q);
+            if (!drained) count_error(p.error_count);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         // The whole warp runs the loop with warp-uniform descriptors; one elected lane issues every
@@ -391,6 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++gi;
         }
         if (!ok && lane == 0) count_error(p.error_count);
+        // drain: one more commit tracks every MMA issued so far; tensor memory is freed (below) only after
+        // it arrives, also when the loop above stopped at a timeout with MMAs still running
+        umma_commit_warp(bars.mma_drain());
+        if (!wait_all(bars.mma_drain(), 0) && lane == 0) count_error(p.error_count);
         __syncwarp();
     } else {
         // ============================================================ softmax / epilogue

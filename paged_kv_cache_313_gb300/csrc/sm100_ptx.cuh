@@ -67,13 +67,57 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete; false after kSpinLimit polls
-// (a few seconds at most).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Wait for phase `parity` of `bar` to complete; false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
+
+// Wait for phase `parity` of `bar` to complete; false after kSpinLimit polls
+// (a few seconds at most).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_bounded(bar, parity, kSpinLimit);
+}
+
+// The same wait taken by a whole warp, with one answer for every lane.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
+
+// Before a CTA exits (or frees tensor memory) every asynchronous copy it issued
+// must have landed: a bulk copy still in flight would write into shared memory
+// that the next CTA on the SM may own.  A ring of `stages` barriers whose
+// phases were armed `armed` times in order (arming n used barrier n % stages,
+// phase n / stages) is drained by waiting for the last armed phase of each
+// barrier; phases that a consumer already waited for return at once.  Returns
+// false if a wait gave up (after kSpinLimit polls).  Called by one thread.
+__device__ __forceinline__ bool drain_ring(uint64_t* bars, uint32_t stages, uint32_t armed) {
+    bool ok = true;
+    for (uint32_t i = 0; i < stages && i < armed; ++i) {
+        const uint32_t last = i + stages * ((armed - 1 - i) / stages);  // the last arming of barrier i
+        ok = mbar_wait(&bars[i], (last / stages) & 1) && ok;
+    }
+    return ok;
+}
+
+// A barrier among `count` warps of a CTA built on an mbarrier (initialised with
+// count `count`), so that the wait is bounded like every other wait: a named
+// barrier (bar.sync) cannot time out, and a warp that has left after a timeout
+// would leave the others waiting on it for ever.  Each warp keeps its own
+// phase counter; every warp must take the same sequence of syncs.
+struct BoundedWarpBarrier {
+    uint64_t* bar;
+    uint32_t phase;
+    // false (for every lane) when the other warps did not arrive within kSpinLimit polls
+    __device__ __forceinline__ bool sync() {
+        __syncwarp();  // the warp's writes precede the release of its arrival
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+        const bool ok = mbar_wait_warp(bar, phase & 1);
+        ++phase;
+        return ok;
+    }
+};
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -21,7 +21,8 @@ PA_F32, PA_BF16 = 0, 1
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
            "pa_write_kv_paged", "pa_write_kv_paged_fp8", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_fp8", "pa_decode_write",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
-           "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy")
+           "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy",
+           "pa_check_bounded_wait")
 
 
 class PaError(RuntimeError):
@@ -57,6 +58,7 @@ _SIGNATURES = {
     "pa_prefill_chunk": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _f, _p,
                           _sz, _p, _p], _i),
     "pa_stage_copy": ([_p, _p, _sz, _p], _i),
+    "pa_check_bounded_wait": ([_i, _i, _p, _p, _p], _i),
     "pa_map_to_kernel_blocks": ([_p, _i, _i, _i, _p, _i, _p], _i),
     "pa_copy_blocks": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _i, _p, _p], _i),
 }
@@ -382,3 +384,17 @@ def pa_map_to_kernel_blocks(mgr_tables, ratio: int, kernel_tables=None, stream=N
         _dev(mgr_tables, "mgr_tables", torch.int32), S, W, int(ratio),
         _dev(kernel_tables, "kernel_tables", torch.int32), kernel_tables.shape[1], _stream(stream)))
     return kernel_tables
+
+
+def pa_check_bounded_wait(polls: int, arrive: bool, device="cuda", stream=None):
+    """Run the library's bounded-wait self-check: one warp waits `polls` polls on an mbarrier that nothing
+    arrives on (arrive=False) or that it arrived on first.  Returns (result, errors) after synchronising:
+    result 1 if the wait succeeded, 0 if it gave up; errors the count it added."""
+    result = torch.full((1,), -1, dtype=torch.int32, device=device)
+    errors = torch.zeros(1, dtype=torch.int32, device=device)
+    _check("pa_check_bounded_wait", lib().pa_check_bounded_wait(int(polls), 1 if arrive else 0,
+                                                                _dev(result, "result", torch.int32),
+                                                                _dev(errors, "error_count", torch.int32),
+                                                                _stream(stream)))
+    torch.cuda.synchronize(result.device)
+    return int(result.item()), int(errors.item())

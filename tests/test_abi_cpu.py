@@ -67,6 +67,19 @@ def test_host_side_rejections_need_no_device(lib):
     assert lib.pa_decode_cascade(*cas) == pa.PA_ERR_UNSUPPORTED
     cas[5], cas[6] = 96, pa.PA_BF16
     assert lib.pa_decode_cascade(*cas) == pa.PA_ERR_UNSUPPORTED
+    # the no-alloc decode takes exactly the shapes pa_decode takes (one shared check)
+    na = [None, None, 1, 8, 8, 96, pa.PA_BF16, None, None, 1, 16, None, 1, None, 16, ctypes.c_float(1.0), None, None]
+    assert lib.pa_decode_noalloc(*na) == pa.PA_ERR_UNSUPPORTED
+    na[3], na[4], na[5] = 3, 2, 128
+    assert lib.pa_decode_noalloc(*na) == pa.PA_ERR_INVALID_ARG
+    na[3], na[4], na[10] = 8, 8, 2048
+    assert lib.pa_decode_noalloc(*na) == pa.PA_ERR_UNSUPPORTED
+    args[3], args[4], args[10] = 8, 8, 2048
+    assert lib.pa_decode(*args) == pa.PA_ERR_UNSUPPORTED
+    # the bounded-wait self-check: poll limit and result pointer are checked on the host
+    assert lib.pa_check_bounded_wait(0, 0, ctypes.c_void_p(16), None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_check_bounded_wait(1 << 17, 0, ctypes.c_void_p(16), None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_check_bounded_wait(100, 0, None, None, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 0, None, None) == pa.PA_OK
     assert lib.pa_copy_blocks(None, None, 4, 16, 8, 128, pa.PA_BF16, None, None, None, 2, None, None) == \
         pa.PA_ERR_INVALID_ARG

@@ -672,3 +672,19 @@ def test_fp8_decode_shapes(case):
     err = _maxabs(st.out_decode, exp.out_decode)
     assert err <= TOL[torch.bfloat16], f"fp8 decode max-abs error {err}"
     assert st.errors() == 0
+
+
+def test_bounded_wait_gives_up_counts_an_error_and_leaves_the_context_usable():
+    """The wait every kernel uses on its mbarriers is bounded: on a barrier nothing arrives on, it gives up
+    after its poll limit, reports false and counts an error, and the kernel returns normally; with the arrival
+    it succeeds.  The context stays usable: a decode right after matches the oracle."""
+    assert pa.pa_check_bounded_wait(256, arrive=False) == (0, 1)
+    assert pa.pa_check_bounded_wait(256, arrive=True) == (1, 0)
+    assert pa.pa_check_bounded_wait(1, arrive=False) == (0, 1)
+    w = W.tiny_fp32(0)
+    exp = expected_step(w)
+    st = DeviceStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert _maxabs(st.out_decode, exp.out_decode) <= 1e-5
+    assert st.errors() == 0
