@@ -211,10 +211,12 @@ PA_API int pa_decode(void* out, const void* q, int num_seqs, int num_q_heads, in
  *     are plain decode);
  *   - prefix_lens: int32 [num_seqs], the number of leading context tokens a
  *     sequence shares with its group (0: none).  All members of a group must
- *     have the same prefix length and the same K/V for those tokens (the same
- *     physical blocks, or copy-on-write copies of them); the prefix is read
- *     through the group's first member's block table, and a member whose
- *     prefix length differs from the first member's is counted in error_count.
+ *     have the same prefix length and map the same physical blocks for those
+ *     tokens (a block copied on write is private and belongs to the tail); the
+ *     prefix is read through the group's first member's block table.  A member
+ *     whose prefix length differs from the first member's, or whose table
+ *     differs from the first member's over the prefix's blocks, is counted in
+ *     error_count (its output is then not its own prefix's).
  *   - max_group_size >= the largest group.
  * Two kernels run on `stream`: the decode kernel, whose queue holds one item
  * per (group, kv head) for the shared prefix (the group's G x members query

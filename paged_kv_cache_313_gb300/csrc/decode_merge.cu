@@ -10,6 +10,14 @@
 // cascade (pa_decode_cascade) slot 0 holds the shared prefix's partial and the
 // tail's partitions follow it.
 //
+// The prefix is read through the group's first member's block table, so in
+// a cascade every member must map the same physical blocks over its prefix
+// ("什么是 PagedAttention？", 共享但不污染状态: branches share the prefix's
+// blocks; a block copied on write is private and belongs to the tail).  The
+// warp of each grouped sequence's head 0 checks that against the tables and
+// counts a member that breaks it in error_count (its output then used the
+// first member's K/V for the prefix).
+//
 // One warp per (sequence, query head) at a time, grid-stride over all of
 // them (a grid of at most a few CTAs per SM, so sequences with a single
 // partition cost one length check, not a CTA).  Each lane holds the weights
@@ -102,6 +110,26 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
             out[1] = from_float<T>(acc.y);
             out[2] = from_float<T>(acc.z);
             out[3] = from_float<T>(acc.w);
+        }
+        if (h == 0 && pre > 0 && p.check_groups != nullptr) {
+            // the first member of s's group (groups are ranges [check_groups[g], check_groups[g + 1]))
+            int first = -1;
+            for (int g0 = 0; g0 < p.check_num_groups && first < 0; g0 += 32) {
+                const int gi = g0 + lane;
+                const int lo = gi < p.check_num_groups ? p.check_groups[gi] : 0;
+                const int hi = gi < p.check_num_groups ? p.check_groups[gi + 1] : 0;
+                const unsigned hit = __ballot_sync(0xffffffffu, lo <= s && s < hi);
+                if (hit) first = __shfl_sync(0xffffffffu, lo, __ffs(hit) - 1);
+            }
+            if (first >= 0 && first != s) {
+                const int nb = (pre + p.block_size - 1) / p.block_size;  // blocks holding prefix tokens
+                const int32_t* mine = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+                const int32_t* ref = p.block_tables + (size_t)first * p.max_blocks_per_seq;
+                bool differ = false;
+#pragma unroll 4
+                for (int b = lane; b < nb; b += 32) differ |= __ldg(mine + b) != __ldg(ref + b);
+                if (__any_sync(0xffffffffu, differ) && lane == 0) count_error(p.error_count);
+            }
         }
     }
 }

@@ -529,6 +529,8 @@ int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_heads, i
     p.scale_log2 = scale * 1.4426950408889634f;
     p.prefix_lens = prefix_lens;
     p.split_base = 1;
+    p.check_groups = num_groups > 0 ? group_offsets : nullptr;
+    p.check_num_groups = num_groups;
 
     PrefillParams pp;
     pp.out = nullptr;

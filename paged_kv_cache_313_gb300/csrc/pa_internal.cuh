@@ -93,6 +93,10 @@ struct DecodeParams {
     // prefix_lens[group_offsets[g]] leading tokens; the decode kernel reads them once per group.
     const int32_t* group_offsets = nullptr;
     int num_groups = 0;
+    // Cascade (either prefix path): the groups again, for the merge kernel's check that every member maps the
+    // first member's physical blocks over its shared prefix (a member that does not is counted in error_count).
+    const int32_t* check_groups = nullptr;
+    int check_num_groups = 0;
     // pa_decode_write: the newest token of each sequence (position L - 1) has its K and V rows in
     // k_new / v_new [num_seqs][num_kv_heads][head_dim]; the decode kernel writes them into the pools
     // (k_write / v_write = k_cache / v_cache) and attends with them; new_slots[s] gets the slot.

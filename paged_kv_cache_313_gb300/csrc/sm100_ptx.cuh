@@ -67,6 +67,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// One non-blocking poll (the thread is never suspended): for waits that are
+// expected to end within a few hundred cycles, where the wake-up latency of a
+// suspended wait would dominate.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kPollLimit = 1u << 24;  // non-blocking polls before a short wait gives up (well under a second)
+
 // Wait for phase `parity` of `bar` to complete; false after `limit` polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
     for (uint32_t i = 0; i < limit; ++i)
@@ -109,13 +125,16 @@ __device__ __forceinline__ bool drain_ring(uint64_t* bars, uint32_t stages, uint
 struct BoundedWarpBarrier {
     uint64_t* bar;
     uint32_t phase;
-    // false (for every lane) when the other warps did not arrive within kSpinLimit polls
+    // false (for every lane) when the other warps did not arrive within kPollLimit polls.  The wait polls
+    // without suspending: the warps of a barrier arrive close together, and a suspended waiter would be
+    // woken late (measured: a suspended wait here cost the prefill epilogue 4-6 us per launch).
     __device__ __forceinline__ bool sync() {
         __syncwarp();  // the warp's writes precede the release of its arrival
         if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-        const bool ok = mbar_wait_warp(bar, phase & 1);
+        bool done = false;
+        for (uint32_t i = 0; i < kPollLimit && !done; ++i) done = mbar_test_wait(bar, phase & 1);
         ++phase;
-        return ok;
+        return __all_sync(0xffffffffu, done) != 0;
     }
 };
 

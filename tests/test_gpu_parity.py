@@ -688,3 +688,38 @@ def test_bounded_wait_gives_up_counts_an_error_and_leaves_the_context_usable():
     torch.cuda.synchronize()
     assert _maxabs(st.out_decode, exp.out_decode) <= 1e-5
     assert st.errors() == 0
+
+
+def test_cascade_counts_a_member_whose_table_breaks_the_group():
+    """A group's prefix is read through its first member's table, so every member must map the same physical
+    blocks over the prefix ("什么是 PagedAttention？", 共享但不污染状态).  A caller's group in which one member
+    maps a different (valid) block inside the prefix is counted in error_count; the other sequences' outputs
+    still match the oracle."""
+    w = W.shared_prefix_bf16(3, num_prompts=3, branches=5, prefix_len=100, max_tail=70, B=16, name="cascade_bad")
+    cas = DeviceStep(w)
+    assert cas.use_cascade
+    cas.slot_mapping()
+    cas.write_kv()
+    torch.cuda.synchronize()
+    goff = w.group_offsets.tolist()
+    s = goff[0] + 1  # the group's second member
+    assert goff[1] - goff[0] >= 2 and int(w.prefix_lens[s]) >= 32
+    bt = w.block_tables.clone()
+    other = int(bt[goff[1], 0])  # a valid block of another prompt, not in this group's prefix
+    assert other not in bt[goff[0], :4].tolist()
+    bt[s, 1] = other
+    cas.block_tables.copy_(bt.to(cas.block_tables.device))
+    got = cas.decode().clone()
+    torch.cuda.synchronize()
+    assert cas.errors() >= 1
+    nd = w.num_decode
+    want = oracle.decode(storage_numpy(w.q_decode), storage_numpy(cas.k_cache.cpu()), storage_numpy(cas.v_cache.cpu()),
+                         bt.numpy()[:nd], w.context_lens.numpy()[:nd], w.scale)
+    keep = [i for i in range(nd) if i != s]
+    assert _maxabs(got[keep], want[keep]) <= TOL[w.dtype]
+    # the consistent batch counts nothing
+    cas.block_tables.copy_(w.block_tables.to(cas.block_tables.device))
+    cas.error_count.zero_()
+    cas.decode()
+    torch.cuda.synchronize()
+    assert cas.errors() == 0
