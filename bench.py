@@ -13,7 +13,12 @@ sequence per step) over all ranks, timed over exactly K steps, each a replay
 of the step captured as a CUDA graph (``--no-graph``: eager launches).  The
 roofline object describes the pa_decode call — the decode kernel and its
 split-KV merge kernel — (algorithmic K/V bytes per call / its CUDA-event
-time over eager launches, against the measured HBM copy bandwidth).  ``e2e`` re-times the step through the public API from host
+time over eager launches after the L2 flush, against the measured HBM copy
+bandwidth).  The line also carries a
+sustained leg (the headline step, flushed, back to back for about 1.5 s, with
+the clock samples taken during it) and, under ``workloads``, the same
+measurements for every other configuration at ``--sweep-steps`` steps each,
+with an oracle sample per configuration.  ``e2e`` re-times the step through the public API from host
 memory: the step's packed inputs copied in from pinned memory (one copy), the
 step (graph replay unless ``--no-graph``), the packed outputs copied back (one
 copy), all inside the events.
@@ -338,6 +343,9 @@ def launches_per_step(step, w, pa):
 def decode_kernel_name(step, w):
     if step.use_cascade:
         return "pa_decode_cascade (decode_tc_kernel: shared-prefix items + tails; decode_merge_kernel)"
+    if w.kv_fp8 and step.fused_decode_write:
+        return ("pa_decode_write_fp8 (decode_tc_kernel over e4m3 pools with the decode tokens' quantising write + "
+                "decode_merge_kernel)")
     if w.kv_fp8:
         return "pa_decode_fp8 (decode_tc_kernel over e4m3 pools + decode_merge_kernel)"
     if step.fused_decode_write:
@@ -408,12 +416,16 @@ def measure(w, args, dev, flush, K, graph=True, sustained_s=0.0, sampler=None, b
     t1 = time.time()
     step_ms = [a.elapsed_time(b) for a, b in ev]
 
-    # ---- per-kernel times (eager launches, same flush) for the roofline
+    # ---- per-stage times for the roofline: eager launches between events, same flush.  After the flush the
+    # GPU spins for a while (a device-side sleep) so that the host has enqueued every stage before the first
+    # event is reached: no host launch gap falls inside a stage's interval (without it, a short kernel in front
+    # of the decode call left the decode's interval up to 15 % long on some runs)
     K1 = max(3, min(K, 100))
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K1)]
     for i in range(K1):
         e = kev[i]
         flush(i & 0xFF)
+        torch.cuda._sleep(400_000)  # ~0.2 ms of GPU cycles, outside the events
         e[0].record(stream)
         step.write_stage()
         e[1].record(stream)
@@ -483,7 +495,8 @@ def measure(w, args, dev, flush, K, graph=True, sustained_s=0.0, sampler=None, b
 def roofline_of(w, step, mean_dec, hbm, peak_kind):
     alg_bytes = decode_algorithmic_bytes(w)  # each physical K/V slot once
     if step.fused_decode_write:  # the decode tokens' new K/V rows: read from k_new/v_new, written to the pools
-        alg_bytes += 2 * w.num_decode * w.kv_bytes_per_token()
+        # (e4m3 pools: the rows are read as bf16, twice the bytes of the codes written)
+        alg_bytes += (3 if w.kv_fp8 else 2) * w.num_decode * w.kv_bytes_per_token()
     logical_bytes = decode_algorithmic_bytes(w, unique=False)  # every sequence's whole context
     achieved = alg_bytes / (mean_dec * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": decode_kernel_name(step, w), "achieved": achieved, "peak": hbm,
@@ -566,7 +579,8 @@ def run_native(args):
                        / (mean_step * 1e-3) / 1e9,
         "roofline": roofline_of(w, step, mean_dec, hbm, peak_kind),
         "stage_ms": {"kv_write (separate launch)": statistics.mean(r["write_ms"]), "decode": mean_dec,
-                     "prefill": statistics.mean(r["prefill_ms"])},
+                     "prefill": statistics.mean(r["prefill_ms"]),
+                     "how": "eager launches between events, after the flush and a device-side wait"},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": mean_e2e, "steps": r["K2"],
                 "launch": "cuda_graph" if args.graph else "eager"},

@@ -279,6 +279,31 @@ PA_API int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_hea
                            void* stream);
 
 /*
+ * pa_decode_fp8 fused with the quantising KV write of the step's decode
+ * tokens: sequence s's newest token (position L-1) has its bf16 K and V rows in
+ * k_new / v_new ([num_seqs][num_kv_heads][head_dim], read).  The decode kernel
+ * stores them into the e4m3 pools k_cache / v_cache at the slot the block
+ * table gives, as code = e4m3(x * (1/k_scale)) and e4m3(x * (1/v_scale)) with
+ * the reciprocal and the product rounded to float (exactly what
+ * pa_write_kv_paged_fp8 stores), and attends with those codes, so the step
+ * needs no separate write launch for its decode tokens ("KV cache 显存管理…",
+ * KV size formula: dtype_size a free factor; 对 ModelRunner 的影响: the write
+ * slots and the attention inputs arrive together).  new_slots (int64
+ * [num_seqs], may be NULL) receives the slots.  Everything else is
+ * pa_decode_fp8's: same shapes, scales, workspace and error behaviour; a
+ * sequence whose newest token falls in a block with an invalid table entry is
+ * counted in error_count and nothing is written for it.  k_scale and v_scale
+ * must be positive and finite (else PA_ERR_INVALID_ARG); k_new and v_new
+ * 16-byte aligned (else PA_ERR_UNSUPPORTED).
+ */
+PA_API int pa_decode_write_fp8(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads,
+                               int head_dim, void* k_cache, void* v_cache, int num_blocks, int block_size,
+                               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                               int max_context_len, float scale, float k_scale, float v_scale, const void* k_new,
+                               const void* v_new, int64_t* new_slots, void* workspace, size_t workspace_bytes,
+                               int32_t* error_count, void* stream);
+
+/*
  * pa_decode for callers that cannot allocate device memory.  The pages have
  * no counterpart: this is a deployment aid, not part of the method.
  *

@@ -389,10 +389,12 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 const unsigned long long valid = __shfl_sync(0xffffffffu, lvalid, l);
                 uint32_t bytes = (uint32_t)__shfl_sync(0xffffffffu, lnvb, l) * block_bytes;
                 if (st == 0 && !d.grouped) bytes += (uint32_t)(C::kHeads * G * D * 2);
-                // pa_decode_write: the sequence's newest token (position L - 1) falls in this stage
+                // pa_decode_write(_fp8): the sequence's newest token (position L - 1) falls in this stage.  bf16
+                // pools: its K and V rows are staged next to the stage; e4m3 pools: the consumer warp that owns
+                // the row loads and quantises them itself (the rows are prefetched into L2 here)
                 int new_row = -1;
                 long long new_slot = -1;
-                if (C::kNewBytes && p.k_new && !d.grouped) {
+                if ((C::kNewBytes || kFp8) && p.k_new && !d.grouped) {
                     const int jn = d.L - 1 - (d.j0 + t0);
                     const bool here = d.L > 0 && jn >= 0 && jn < nt;
                     const int pbn = __shfl_sync(0xffffffffu, pb_lane, (b0 + (here ? jn / B : 0)) & 31);
@@ -400,6 +402,12 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                         new_row = jn;
                         new_slot = (long long)pbn * B + (d.L - 1) % B;
                         bytes += (uint32_t)C::kNewBytes;
+                        if (kFp8 && lane < 4 * C::kHeads) {  // K and V rows of each kv head: 256 bytes, 2 lines each
+                            const int hh = lane >> 2, isv = (lane >> 1) & 1, half = lane & 1;
+                            const __nv_bfloat16* row = static_cast<const __nv_bfloat16*>(isv ? p.v_new : p.k_new) +
+                                                       ((size_t)d.s * Hkv + d.kvh + hh) * D + half * 64;
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+                        }
                     }
                 }
                 if (lane == 0) {
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     inf.new_row = new_row;
                     inf.new_slot = new_slot;
                     mbar_arrive_expect_tx(&full[slot], bytes);
-                    if (new_row >= 0) {
+                    if (C::kNewBytes && new_row >= 0) {  // bf16 pools: stage the newest token's rows
                         const size_t row = ((size_t)d.s * Hkv + d.kvh) * D;
                         bulk_load(smem + C::kNew + slot * C::kNewBytes,
                                   static_cast<const __nv_bfloat16*>(p.k_new) + row, (uint32_t)(D * 2), &full[slot]);
@@ -560,6 +568,26 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             }
             uint8_t* kt = smem + C::kRing + slot * C::kStageBytes;
             uint8_t* vt = kt + C::kTileBytes;
+            // pa_decode_write_fp8: the newest token's K and V rows of this warp's kv head, when the token is one of
+            // rows [rlo, rhi) of the stage, quantised here (code = e4m3(x * (1/scale)), four elements per lane)
+            // into the tiles, before any ldmatrix of the row, and into the pools at its slot
+            auto patch_new_fp8 = [&](int rlo, int rhi) {
+                if (!kFp8 || inf.new_row < rlo || inf.new_row >= rhi) return;
+                const int kvh_h = inf.kvh + hp;
+                const size_t roff = ((size_t)inf.s * Hkv + kvh_h) * D;
+                const uint2 kx = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.k_new) + roff) + lane);
+                const uint2 vx = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.v_new) + roff) + lane);
+                const uint32_t kc = e4m3x4_of_bf16x4(kx, p.k_inv), vc = e4m3x4_of_bf16x4(vx, p.v_inv);
+                const uint32_t off = tr.at(inf.new_row, hp, lane >> 2) + (lane & 3) * 4;
+                *reinterpret_cast<uint32_t*>(kt + off) = kc;
+                *reinterpret_cast<uint32_t*>(vt + off) = vc;
+                const size_t poff = ((size_t)inf.new_slot * Hkv + kvh_h) * D;
+                reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.k_write) + poff)[lane] = kc;
+                reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.v_write) + poff)[lane] = vc;
+                if (p.new_slots && kvh_h == 0 && lane == 0) p.new_slots[inf.s] = inf.new_slot;
+                fence_proxy_async_smem();  // these writes precede the slot's next TMA write
+                __syncwarp();
+            };
             // 16 token rows r0c..r0c+15 of the stage against this warp's 8 query rows (validity `rows`)
             auto chunk16 = [&](const int r0c, const uint32_t rows) {
                 if (rows != 0xFFFFu) {  // zero V rows without a valid token
@@ -675,13 +703,16 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 for (int r0c = 0; r0c < inf.ntok; r0c += 16) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
             } else if constexpr (C::kHeads == 2) {
                 // two chunks of 16 rows of this warp's head
+                if (p.k_new) patch_new_fp8(row0, row0 + 32);
 #pragma unroll 1
                 for (int c = 0; c < 2; ++c) {
                     const int r0c = row0 + 16 * c;
                     if (r0c < inf.ntok) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
                 }
             } else if (row0 < inf.ntok) {
-                if (inf.new_row >= row0 && inf.new_row < row0 + 16) {
+                if (kFp8) {
+                    if (p.k_new) patch_new_fp8(row0, row0 + 16);
+                } else if (inf.new_row >= row0 && inf.new_row < row0 + 16) {
                     // pa_decode_write: the newest token's staged K and V rows go into this stage's tiles
                     // (128-byte swizzled, before any ldmatrix of the row) and into the pool at its slot
                     const uint8_t* stg = smem + C::kNew + slot * C::kNewBytes;
@@ -939,8 +970,8 @@ int pool_tensor_map_rows(CUtensorMap* map, const void* pool, int num_blocks, int
 bool decode_tc_supported(const DecodeParams& p, int dtype) {
     const int B = p.block_size;
     if (dtype != PA_BF16 || (p.head_dim != 64 && p.head_dim != 128) || p.group > 8) return false;
-    // fp8 pools: head_dim 128, plain decode (no cascade items, no fused write)
-    if (p.kv_fp8 && (p.head_dim != 128 || p.group_offsets || p.k_new)) return false;
+    // fp8 pools: head_dim 128, plain decode or the fused write (no cascade items)
+    if (p.kv_fp8 && (p.head_dim != 128 || p.group_offsets)) return false;
     if (B != 8 && B != 16 && B != 32 && B != 64) return false;
     if (p.partition % 64 != 0 || p.num_seqs > kMaxSeqsPersistent) return false;
     if (((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) || ((uintptr_t)p.q & 15) || ((uintptr_t)p.out & 15))

@@ -105,14 +105,6 @@ __global__ void write_kv_kernel(const int4* __restrict__ k_new, const int4* __re
     }
 }
 
-// Two floats to their nearest e4m3 codes (ties to even, saturating at 448),
-// packed as {lo: byte 0, hi: byte 1}.
-__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
-    uint16_t d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-
 // pa_write_kv_paged_fp8: slot mapping, then each bf16 element x of the token's
 // K and V rows stored as e4m3(x * inv_scale) into uint8 pools.  One CTA per
 // token; a thread converts eight elements (16 bytes in, 8 bytes out).
@@ -140,14 +132,8 @@ __global__ void write_kv_paged_fp8_kernel(const uint4* __restrict__ k_new, const
         const int j = isv ? i - row_vec8 : i;
         const uint4 x = isv ? __ldg(v_new + (long long)t * row_vec8 + j) : __ldg(k_new + (long long)t * row_vec8 + j);
         const float inv = isv ? v_inv : k_inv;
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint16_t q[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-            q[k] = pack_e4m3x2(__fmul_rn(lo, inv), __fmul_rn(hi, inv));
-        }
-        const uint2 out = make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+        const uint2 out = make_uint2(e4m3x4_of_bf16x4(make_uint2(x.x, x.y), inv),
+                                     e4m3x4_of_bf16x4(make_uint2(x.z, x.w), inv));
         (isv ? v_cache : k_cache)[slot * row_vec8 + j] = out;
     }
 }

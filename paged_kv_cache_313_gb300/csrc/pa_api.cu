@@ -397,6 +397,38 @@ int pa_decode_write(void* out, const void* q, int num_seqs, int num_q_heads, int
     return run_decode(p, dtype, num_sms, static_cast<cudaStream_t>(stream));
 }
 
+int pa_decode_write_fp8(void* out, const void* q, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        void* k_cache, void* v_cache, int num_blocks, int block_size, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, float scale,
+                        float k_scale, float v_scale, const void* k_new, const void* v_new, int64_t* new_slots,
+                        void* workspace, size_t workspace_bytes, int32_t* error_count, void* stream) {
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 && num_blocks >= 0 && max_blocks_per_seq >= 0 && max_context_len >= 0 &&
+        decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size) == PA_OK)
+        return PA_OK;
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_UNSUPPORTED;
+    DecodeParams p;
+    int num_sms = 0;
+    int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, PA_BF16, k_cache,
+                            v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, scale, workspace, workspace_bytes, error_count);
+    if (rc != PA_OK) return rc;
+    p.kv_fp8 = 1;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.k_inv = 1.0f / k_scale;  // in float, as the separate quantising write computes it
+    p.v_inv = 1.0f / v_scale;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_write = k_cache;
+    p.v_write = v_cache;
+    p.new_slots = new_slots;
+    if (!decode_tc_supported(p, PA_BF16)) return PA_ERR_UNSUPPORTED;
+    return run_decode(p, PA_BF16, num_sms, static_cast<cudaStream_t>(stream));
+}
+
 size_t pa_prefill_workspace_size(int num_chunks, int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size) {
     (void)num_chunks; (void)max_q_len; (void)num_q_heads; (void)num_kv_heads; (void)head_dim; (void)block_size;

@@ -108,6 +108,9 @@ struct DecodeParams {
     // fp8 pools: k_cache / v_cache hold e4m3 codes read back as code * k_scale / code * v_scale
     int kv_fp8 = 0;
     float k_scale = 1.f, v_scale = 1.f;
+    // fp8 pools with a fused write (k_new set): the new rows are stored as e4m3(x * k_inv) / e4m3(x * v_inv),
+    // the reciprocals computed in float on the host as the separate quantising write computes them
+    float k_inv = 1.f, v_inv = 1.f;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;
@@ -194,6 +197,23 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Two floats to their nearest e4m3 codes (ties to even, magnitudes beyond 448 held at 448), lo in the low byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Four bf16 values (two 32-bit words, element 0 in the low half of x.x) to four e4m3 codes of x * inv, the
+// product rounded to float: the fp8 pools' stored form, code = e4m3(x * (1/scale)).
+__device__ __forceinline__ uint32_t e4m3x4_of_bf16x4(uint2 x, float inv) {
+    const uint16_t a = pack_e4m3x2(__fmul_rn(__uint_as_float(x.x << 16), inv),
+                                   __fmul_rn(__uint_as_float(x.x & 0xFFFF0000u), inv));
+    const uint16_t b = pack_e4m3x2(__fmul_rn(__uint_as_float(x.y << 16), inv),
+                                   __fmul_rn(__uint_as_float(x.y & 0xFFFF0000u), inv));
+    return (uint32_t)a | ((uint32_t)b << 16);
 }
 
 __device__ __forceinline__ void count_error(int32_t* error_count, int n = 1) {

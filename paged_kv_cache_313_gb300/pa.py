@@ -20,6 +20,7 @@ PA_F32, PA_BF16 = 0, 1
 # Every symbol include/pa.h declares.
 SYMBOLS = ("pa_version", "pa_status_string", "pa_last_cuda_error", "pa_slot_mapping", "pa_write_kv",
            "pa_write_kv_paged", "pa_write_kv_paged_fp8", "pa_decode_workspace_size", "pa_decode_plan", "pa_decode", "pa_decode_fp8", "pa_decode_write",
+           "pa_decode_write_fp8",
            "pa_decode_cascade_workspace_size", "pa_decode_cascade", "pa_decode_noalloc", "pa_prefill_workspace_size",
            "pa_prefill_chunk", "pa_copy_blocks", "pa_map_to_kernel_blocks", "pa_stage_copy",
            "pa_check_bounded_wait")
@@ -48,6 +49,8 @@ _SIGNATURES = {
     "pa_decode_plan": ([_i, _i, _i, _i, _i, _i, _p, _p], _i),
     "pa_decode": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _sz, _p, _p], _i),
     "pa_decode_fp8": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _f, _f, _p, _sz, _p, _p], _i),
+    "pa_decode_write_fp8": ([_p, _p, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _f, _f, _p, _p, _p, _p, _sz,
+                             _p, _p], _i),
     "pa_decode_write": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _i, _i, _p, _i, _p, _i, _f, _p, _p, _p, _p, _sz, _p,
                          _p], _i),
     "pa_decode_cascade_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
@@ -243,6 +246,31 @@ def pa_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_l
         _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale), float(k_scale),
         float(v_scale), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dev(error_count, "error_count", torch.int32), _stream(stream)))
+    return out
+
+
+def pa_decode_write_fp8(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int, scale: float,
+                        k_scale: float, v_scale: float, k_new, v_new, workspace, out=None, new_slots=None,
+                        error_count=None, stream=None) -> torch.Tensor:
+    """pa_decode_fp8 that also stores each sequence's newest token (bf16 K/V rows k_new/v_new [N, Hkv, D]) into the
+    e4m3 pools at its slot, quantised as e4m3(x * (1/scale)), in the same launch."""
+    N, Hq, D = q.shape
+    P, B, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(k_new.shape) != (N, Hkv, D) or tuple(v_new.shape) != (N, Hkv, D):
+        raise ValueError("shapes of q, k_cache, k_new, v_new disagree")
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("fp8 pools are uint8 tensors of e4m3 codes")
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pa_decode_write_fp8", lib().pa_decode_write_fp8(
+        _dev(out, "out", torch.bfloat16, host_ok=True),
+        _dev(q, "q", torch.bfloat16), N, Hq, Hkv, D, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), P, B,
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), float(scale), float(k_scale),
+        float(v_scale), _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16),
+        _dev(new_slots, "new_slots", torch.int64), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dev(error_count, "error_count", torch.int32),
+        _stream(stream)))
     return out
 
 

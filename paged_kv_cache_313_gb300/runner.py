@@ -77,13 +77,14 @@ class DeviceStep:
         self.cascade_workspace = (pa.new_cascade_workspace(nd, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                                            w.block_size, self.max_context_len, device=dev)
                                   if self.use_cascade else None)
-        # decode tokens written by the decode kernel itself (pa_decode_write) when the step's first nd new
+        # decode tokens written by the decode kernel itself (pa_decode_write, pa_decode_write_fp8) when the step's first nd new
         # tokens are the decode sequences' newest ones and the shapes are the tensor-core decode kernel's
         G = w.num_q_heads // w.num_kv_heads
         newest = bool(nd) and torch.equal(w.seq_idx[:nd], torch.arange(nd, dtype=w.seq_idx.dtype)) and \
             torch.equal(w.pos[:nd], w.context_lens[:nd].to(w.pos.dtype) - 1)
-        self.fused_decode_write = bool(fused_decode_write and newest and not self.use_cascade and not w.kv_fp8
-                                       and w.dtype == torch.bfloat16 and w.head_dim in (64, 128) and G <= 8
+        dims = (128,) if w.kv_fp8 else (64, 128)  # e4m3 pools: the decode kernel takes head_dim 128
+        self.fused_decode_write = bool(fused_decode_write and newest and not self.use_cascade
+                                       and w.dtype == torch.bfloat16 and w.head_dim in dims and G <= 8
                                        and w.block_size in (8, 16, 32, 64))
         n = pa.pa_prefill_workspace_size(w.num_chunks, w.max_q_len, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size) if w.num_chunks else 0
@@ -153,6 +154,11 @@ class DeviceStep:
         if not self.fused_decode_write:
             return self.decode(stream)
         w, nd = self.w, self.w.num_decode
+        if w.kv_fp8:
+            return pa.pa_decode_write_fp8(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
+                                          self.context_lens[:nd], self.max_context_len, w.scale, w.k_scale, w.v_scale,
+                                          self.k_new[:nd], self.v_new[:nd], self.workspace, out=self.out_decode,
+                                          new_slots=self.slots[:nd], error_count=self.error_count, stream=stream)
         return pa.pa_decode_write(self.q_decode, self.k_cache, self.v_cache, self.block_tables[:nd],
                                   self.context_lens[:nd], self.max_context_len, w.scale, self.k_new[:nd],
                                   self.v_new[:nd], self.workspace, out=self.out_decode, new_slots=self.slots[:nd],

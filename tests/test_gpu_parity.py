@@ -627,6 +627,83 @@ def test_fp8_write_of_every_bf16_value_matches_oracle(k_scale, v_scale):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("kind", ["small", "full"])
+def test_decode_write_fp8_equals_separate_write_then_decode(kind):
+    """pa_decode_write_fp8 (the e4m3 decode kernel quantises each sequence's newest token, stores the codes in the
+    pools and attends with them) leaves the same pools and slots as the separate quantising write and gives the
+    same outputs, bit for bit, at the step's full size and reduced."""
+    w, exp = _case(kind, "decode_fp8")
+    fused = DeviceStep(w)
+    assert fused.fused_decode_write
+    plain = DeviceStep(w, fused_decode_write=False)
+    fused.run()
+    plain.run()
+    torch.cuda.synchronize()
+    assert fused.errors() == 0 and plain.errors() == 0
+    assert torch.equal(fused.slots.cpu(), torch.from_numpy(exp.slots))
+    assert torch.equal(fused.k_cache, plain.k_cache) and torch.equal(fused.v_cache, plain.v_cache)
+    assert np.array_equal(fused.k_cache.cpu().numpy(), exp.k_cache)
+    assert np.array_equal(fused.v_cache.cpu().numpy(), exp.v_cache)
+    assert torch.equal(fused.out_decode, plain.out_decode)
+    assert _maxabs(fused.out_decode, exp.out_decode) <= TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 0.37), (1.0 / 64, 3.0), (0.7, 0.9), (0.6, 1.0)])
+def test_fused_fp8_write_of_every_bf16_value_matches_oracle(k_scale, v_scale):
+    """The quantising write inside the e4m3 decode kernel, bit-exact against the oracle for every bf16 bit pattern
+    but the NaNs: 64 sequences x 8 kv heads x 128 columns of newest-token K (and a permutation for V) = 65536
+    elements, at power-of-two scales and at scales whose reciprocal and product round.  Whole pools compared
+    (untouched slots included); the outputs bit-identical to the separate quantising write followed by
+    pa_decode_fp8 (the codes span the whole e4m3 range here, so outputs reach magnitudes where the absolute bf16
+    tolerance of the workloads does not apply)."""
+    N, Hq, H, D, B = 64, 32, 8, 128, 16
+    rng = np.random.default_rng(17)
+    lens = (1 + 5 * np.arange(N)).astype(np.int32)  # the newest token lands at every offset of a block
+    nblk = [oracle.num_blocks(int(L), B) for L in lens]
+    P = sum(nblk) + 7
+    perm = rng.permutation(P).astype(np.int32)
+    bt = np.full((N, max(nblk)), -1, np.int32)
+    o = 0
+    for s_, nb in enumerate(nblk):
+        bt[s_, :nb] = perm[o:o + nb]
+        o += nb
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    bits[((bits & 0x7F80) == 0x7F80) & ((bits & 0x7F) != 0)] = 0
+    k_bits = bits.reshape(N, H, D)
+    v_bits = rng.permutation(bits).reshape(N, H, D)
+    kc0 = (rng.integers(0x30, 0x60, size=(P, B, H, D), dtype=np.uint8) | (rng.integers(0, 2, size=(P, B, H, D), dtype=np.uint8) << 7))
+    vc0 = (rng.integers(0x30, 0x60, size=(P, B, H, D), dtype=np.uint8) | (rng.integers(0, 2, size=(P, B, H, D), dtype=np.uint8) << 7))
+    slots, nerr = oracle.slot_mapping(bt, np.arange(N, dtype=np.int32), lens - 1, B, P)
+    assert nerr == 0
+    k_exp, v_exp = kc0.copy(), vc0.copy()
+    assert oracle.write_kv_fp8(k_bits, v_bits, k_exp, v_exp, slots, k_scale, v_scale) == 0
+    q = torch.from_numpy(rng.standard_normal((N, Hq, D), dtype=np.float32)).to(torch.bfloat16)
+    scale = 1 / math.sqrt(D)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    bf = lambda b: dev(b.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    kc, vc = dev(kc0), dev(vc0)
+    slot_out = torch.full((N,), -7, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = pa.new_decode_workspace(N, Hq, H, D, B, int(lens.max()))
+    out = pa.pa_decode_write_fp8(q.cuda(), kc, vc, dev(bt), dev(lens), int(lens.max()), scale, k_scale, v_scale,
+                                 bf(k_bits), bf(v_bits), ws, new_slots=slot_out, error_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(slot_out.cpu(), torch.from_numpy(slots))
+    assert np.array_equal(kc.cpu().numpy(), k_exp), "K codes differ"
+    assert np.array_equal(vc.cpu().numpy(), v_exp), "V codes differ"
+    kc2, vc2 = dev(kc0), dev(vc0)
+    pa.pa_write_kv_paged_fp8(bf(k_bits), bf(v_bits), kc2, vc2, dev(bt), dev(np.arange(N, dtype=np.int32)),
+                             dev(lens - 1), k_scale, v_scale, error_count=err)
+    ws2 = pa.new_decode_workspace(N, Hq, H, D, B, int(lens.max()))
+    out2 = pa.pa_decode_fp8(q.cuda(), kc2, vc2, dev(bt), dev(lens), int(lens.max()), scale, k_scale, v_scale, ws2,
+                            error_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+    assert torch.equal(out, out2)
+
+
 FP8_DECODE_CASES = [
     # (Hq, Hkv, B, decode context lengths, code range): every block size, groups 1..8, partition boundaries,
     # and codes over the whole finite range (subnormals up to 448) through the in-register conversion; even
