@@ -39,6 +39,11 @@ __device__ __forceinline__ int decode_start(const DecodeParams& p, int s, int L,
     return pre & ~63;
 }
 
+// Tokens per partition of sequence s: the batch's last sequences (from small_from on) use shorter ones.
+__device__ __forceinline__ int partition_of(const DecodeParams& p, int s) {
+    return s >= p.small_from ? p.small_partition : p.partition;
+}
+
 __device__ __forceinline__ size_t decode_unit(const DecodeParams& p, int s, int kvh) {
     return (size_t)s * p.num_kv_heads + kvh;
 }

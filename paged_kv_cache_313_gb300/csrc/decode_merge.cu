@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
         const int s = (int)(u / Hq), h = (int)(u - (long long)s * Hq);
         const int L = decode_context(p, s, false);
         int pre;
-        const int nsplit = num_partitions(L - decode_start(p, s, L, &pre), p.partition);
+        const int nsplit = num_partitions(L - decode_start(p, s, L, &pre), partition_of(p, s));
         if (nsplit <= 1 && pre == 0) continue;  // the decode kernel wrote this output directly
         // partial slots [0, split_base) hold the cascade prefix (valid when pre > 0), then the partitions
         const int first = pre > 0 ? 0 : p.split_base, ntot = p.split_base + nsplit;

@@ -96,6 +96,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, int num_seqs, int num
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_context_len = max_context_len;
     p.partition = plan.partition;
+    p.small_partition = plan.small_partition;
+    p.small_from = plan.small_from;
     p.max_splits = plan.max_splits;
     p.scale_log2 = scale * 1.4426950408889634f;
     return run_decode(p, dtype, num_sms, st);

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     // every sequence's short last partition after all the whole ones was measured 5-7% slower.)
     auto counted_items = [&](int L, int s) {
         int pre;
-        return num_partitions(L - decode_start(p, s, L, &pre), p.partition) * HkvI;
+        return num_partitions(L - decode_start(p, s, L, &pre), partition_of(p, s)) * HkvI;
     };
     {
         const int per = (N + C::kThreads - 1) / C::kThreads;
@@ -307,9 +307,10 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 d.kvh *= C::kHeads;  // the item's first kv head
                 d.L = context_of(d.s);
                 const int j_first = decode_start(p, d.s, d.L, &d.pre);
-                d.nsplit = num_partitions(d.L - j_first, p.partition);
-                d.j0 = j_first + d.split * p.partition;
-                d.ntok = max(0, min(d.L, d.j0 + p.partition) - d.j0);
+                const int part = partition_of(p, d.s);
+                d.nsplit = num_partitions(d.L - j_first, part);
+                d.j0 = j_first + d.split * part;
+                d.ntok = max(0, min(d.L, d.j0 + part) - d.j0);
             }
             return d;
         };
@@ -974,6 +975,7 @@ bool decode_tc_supported(const DecodeParams& p, int dtype) {
     if (p.kv_fp8 && (p.head_dim != 128 || p.group_offsets)) return false;
     if (B != 8 && B != 16 && B != 32 && B != 64) return false;
     if (p.partition % 64 != 0 || p.num_seqs > kMaxSeqsPersistent) return false;
+    if (p.small_from < p.num_seqs && (p.small_partition % 64 != 0 || p.small_partition < 64)) return false;
     if (((uintptr_t)p.k_cache & 15) || ((uintptr_t)p.v_cache & 15) || ((uintptr_t)p.q & 15) || ((uintptr_t)p.out & 15))
         return false;
     if ((long long)p.num_blocks * B >= (1LL << 31)) return false;

@@ -92,9 +92,15 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 #ifndef PA_DECODE_ITEMS_PER_SM
 #define PA_DECODE_ITEMS_PER_SM 0
 #endif
+// Percentage of a batch's sequences, the last ones, cut into quarter-length partitions (0: none).  The
+// tensor-core decode kernel hands out its items sequence by sequence, so these come last: when the queue runs
+// dry each CTA holds a short item, and the CTAs finish closer together.
+#ifndef PA_DECODE_SMALL_TAIL_PCT
+#define PA_DECODE_SMALL_TAIL_PCT 20
+#endif
 
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
-                       int num_sms, size_t workspace_cap) {
+                       int num_sms, size_t workspace_cap, int reserved) {
     // Work items are (sequence, partition, kv head).  PA_DECODE_PARTITION-token
     // partitions (1024: measured against 512 and 2048, it halves the partials
     // a long context leaves to merge and is neutral elsewhere) keep each item's
@@ -115,18 +121,36 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         int sp = (int)(((long long)max_context_len + part - 1) / part);
         return sp < 1 ? 1 : sp;
     };
-    while (splits_of(partition) > 128 && partition < (1 << 29)) partition <<= 1;
-    while (splits_of(partition) > 1 && partition < (1 << 29) &&
-           decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, splits_of(partition)).total >
+    // the last sequences (PA_DECODE_SMALL_TAIL_PCT % of them, rounded up) use quarter-length partitions, as
+    // long as their items, counted at the longest context, stay within four per resident CTA (two per SM):
+    // a few long contexts cut small would add more per-item work than the shorter tail saves
+    auto small_of = [](int part) { return part / 4 < 64 ? 64 : part / 4; };
+    const long long small_items_per_seq = (long long)splits_of(small_of(partition)) * num_kv_heads;
+    long long small_count = ((long long)num_seqs * PA_DECODE_SMALL_TAIL_PCT + 99) / 100;
+    if (small_count * small_items_per_seq > 8LL * num_sms) small_count = 8LL * num_sms / small_items_per_seq;
+    auto slots_of = [&](int part) {  // partial slots per (sequence, kv head)
+        return reserved + (small_count > 0 ? splits_of(small_of(part)) : splits_of(part));
+    };
+    while (slots_of(partition) > 128 && partition < (1 << 29)) partition <<= 1;
+    while (slots_of(partition) > 1 + reserved && partition < (1 << 29) &&
+           decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, slots_of(partition)).total >
                workspace_cap)
         partition <<= 1;
-    return DecodePlan{partition, splits_of(partition)};
+    return DecodePlan{partition, slots_of(partition), small_count > 0 ? small_of(partition) : partition,
+                      num_seqs - (int)small_count};
 }
 
 int run_decode(const DecodeParams& p, int dtype, int num_sms, cudaStream_t stream) {
-    int rc = decode_tc_supported(p, dtype) ? launch_decode_tc(p, num_sms, stream) : launch_decode_fma(p, dtype, stream);
-    if (rc != PA_OK) return rc;
-    return launch_decode_merge(p, dtype, num_sms, stream);
+    if (decode_tc_supported(p, dtype)) {
+        const int rc = launch_decode_tc(p, num_sms, stream);
+        return rc != PA_OK ? rc : launch_decode_merge(p, dtype, num_sms, stream);
+    }
+    // the CUDA-core kernel launches one CTA per (sequence, kv head, partition): uniform partitions (its
+    // workspace, sized for the shorter ones, has room to spare)
+    DecodeParams q = p;
+    q.small_from = 1 << 30;
+    const int rc = launch_decode_fma(q, dtype, stream);
+    return rc != PA_OK ? rc : launch_decode_merge(q, dtype, num_sms, stream);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -326,6 +350,8 @@ static int prepare_decode(DecodeParams* p, int* num_sms, void* out, const void* 
     p->max_blocks_per_seq = max_blocks_per_seq;
     p->max_context_len = max_context_len;
     p->partition = plan.partition;
+    p->small_partition = plan.small_partition;
+    p->small_from = plan.small_from;
     p->max_splits = plan.max_splits;
     p->scale_log2 = scale * 1.4426950408889634f;
     return PA_OK;
@@ -492,13 +518,7 @@ int pa_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens, const i
 // every (sequence, kv head) holds the prefix partial, so max_splits grows by one.
 static DecodePlan plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
                                int num_sms) {
-    DecodePlan pl = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
-    while (pl.max_splits + 1 > 128) {
-        pl.partition <<= 1;
-        pl.max_splits = (int)(((long long)max_context_len + pl.partition - 1) / pl.partition);
-    }
-    pl.max_splits += 1;
-    return pl;
+    return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX, 1);
 }
 
 size_t pa_decode_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -558,6 +578,8 @@ int pa_decode_cascade(void* out, const void* q, int num_seqs, int num_q_heads, i
     p.max_context_len = max_context_len;
     p.partition = plan.partition;
     p.max_splits = plan.max_splits;
+    p.small_partition = plan.small_partition;
+    p.small_from = plan.small_from;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.prefix_lens = prefix_lens;
     p.split_base = 1;

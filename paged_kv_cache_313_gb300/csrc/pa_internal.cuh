@@ -56,12 +56,15 @@ int decode_shape_ok(int num_q_heads, int num_kv_heads, int head_dim, int block_s
 
 // Split-KV partition policy shared by pa_decode and pa_decode_workspace_size.
 struct DecodePlan {
-    int partition;   // tokens per split (multiple of 64)
-    int max_splits;  // ceil(max_context_len / partition)
+    int partition;        // tokens per split (multiple of 64)
+    int max_splits;       // partial slots per (sequence, kv head): the most partitions any sequence can have
+    int small_partition;  // the shorter partitions of the batch's last sequences (multiple of 64)
+    int small_from;       // first sequence cut into small_partition-token partitions (num_seqs: none)
 };
-// `workspace_cap`: largest split-KV scratch the caller can offer (SIZE_MAX: any).
+// `workspace_cap`: largest split-KV scratch the caller can offer (SIZE_MAX: any); `reserved`: partial slots
+// per (sequence, kv head) used before the partitions' (the cascade's prefix slot).
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
-                       int num_sms, size_t workspace_cap);
+                       int num_sms, size_t workspace_cap, int reserved = 0);
 
 // Workspace layout of pa_decode (byte offsets from the 256-aligned base).
 struct DecodeWorkspace {
@@ -114,6 +117,9 @@ struct DecodeParams {
     int num_seqs, num_q_heads, num_kv_heads, head_dim, group;
     int num_blocks, block_size, max_blocks_per_seq, max_context_len;
     int partition, max_splits;
+    // Sequences s >= small_from are cut into small_partition-token partitions instead (the tensor-core
+    // kernel's queue ends with them, so the last items handed out are short); 1 << 30: none.
+    int small_partition = 0, small_from = 1 << 30;
     float scale_log2;  // scale * log2(e): scores are kept in base-2 units
 };
 
