@@ -325,9 +325,9 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
         const uint32_t block_bytes = 2u * C::kSegs * B * 128u;  // K and V of one block and the item's kv heads
         const uint64_t kv_policy = l2_policy_evict_first();  // K/V is read once per call
 
-        int item = 0;
-        if (lane == 0) item = atomicAdd(&work[0], 1);
-        item = __shfl_sync(0xffffffffu, item, 0);
+        // the first item is the CTA's own index (no claim on the way to the first copies); later claims take
+        // the counter's places after the grid's
+        int item = blockIdx.x;
         int nxt = 0;  // the item after this one (lane 0), claimed a few stages before this one's last
         Item d{};
         int raw = -1;
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                                     my_pb * B, d.kvh * C::kHalves, &full[slot]);
                 __syncwarp();
                 ++stage_no;
-                if (st == claim_at && lane == 0) nxt = atomicAdd(&work[0], 1);
+                if (st == claim_at && lane == 0) nxt = (int)gridDim.x + atomicAdd(&work[0], 1);
                 if (st == describe_at) {
                     item2 = __shfl_sync(0xffffffffu, nxt, 0);
                     if (item2 < total) {
