@@ -62,6 +62,7 @@
 // memory when the CTA is gone.  The work counter is reset by the last CTA to
 // finish.
 #include <atomic>
+#include <type_traits>
 
 #include "decode_common.cuh"
 #include "sm100_ptx.cuh"
@@ -184,7 +185,9 @@ __device__ __forceinline__ void decode_item(const int* cum, int N, int Hkv, int 
     kvh = r - split * Hkv;
 }
 
-template <int D, bool kFp8, bool kPair>
+// kPrefix: the cascade's kernel, whose queue begins with shared-prefix items (a separate instantiation, so that
+// the prefix items' four-chunk code does not shape the plain decode kernel's)
+template <int D, bool kFp8, bool kPair, bool kPrefix>
 __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8, kPair>::kCtasPerSm)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const DecodeParams p, int* work) {
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     }
     // items: the cascade groups' shared prefixes (one per group and kv head) first, then the
     // (sequence, partition, kv head) items of the prefix sum
-    const int n_grouped = p.group_offsets ? p.num_groups * Hkv : 0;
+    const int n_grouped = kPrefix && p.group_offsets ? p.num_groups * Hkv : 0;
     const int total = n_grouped + s_total;
 
     if (warp == C::kConsumerWarps) {
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             }
             const StageInfo inf = info[slot];
             if (inf.s < 0) break;
-            if ((inf.flags & 17) == 17) {  // first stage of a shared-prefix item: this warp's 8 rows from global
+            if (kPrefix && (inf.flags & 17) == 17) {  // first stage of a shared-prefix item: this warp's 8 rows from global
                 // row 8*warp + g4 is member (row / G), head (row % G) of the group's first sequence inf.s
                 const int rr = warp * 8 + g4, mem = rr / G, head = rr - mem * G;
                 const bool row_ok = mem < inf.nsplit;
@@ -589,57 +592,83 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 fence_proxy_async_smem();  // these writes precede the slot's next TMA write
                 __syncwarp();
             };
-            // 16 token rows r0c..r0c+15 of the stage against this warp's 8 query rows (validity `rows`)
-            auto chunk16 = [&](const int r0c, const uint32_t rows) {
-                if (rows != 0xFFFFu) {  // zero V rows without a valid token
-                    const int r = lane >> 1;
-                    if (!((rows >> r) & 1u)) {
-                        const int4 z = make_int4(0, 0, 0, 0);
+            // NC chunks of 16 token rows from row r0 of the stage (validity bits in `valid`) against this warp's 8
+            // query rows, in one online-softmax step: the chunks' scores (independent MMA chains), one row max and
+            // one rescale of the output for all of them, then each chunk's P V.  A chunk without a valid token is
+            // skipped (it would add nothing); in one with some, the V rows of invalid tokens are zeroed first.
+            auto chunks = [&](auto nc, const int r0, const unsigned long long valid) {
+                constexpr int NC = decltype(nc)::value;
+                uint32_t rows[NC];
+                bool zeroed = false;
 #pragma unroll
-                        for (int h = 0; h < C::kHalves; ++h)
+                for (int c = 0; c < NC; ++c) {
+                    rows[c] = (uint32_t)(valid >> (r0 + 16 * c)) & 0xFFFFu;  // (r0 + 16 c <= 48)
+                    if (rows[c] != 0u && rows[c] != 0xFFFFu) {  // zero V rows without a valid token
+                        zeroed = true;
+                        const int r = lane >> 1;
+                        if (!((rows[c] >> r) & 1u)) {
+                            const int4 z = make_int4(0, 0, 0, 0);
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<int4*>(vt + tr.row(r0c + r) + (hp * C::kHalves + h) * tr.half_stride +
-                                                         ((lane & 1) * 4 + c) * 16) = z;
-                    }
-                    __syncwarp();
-                }
-                // S^T = K Q^T (two independent accumulation chains)
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (kFp8) {
-                    // one ldmatrix.x4 per 32 e4m3 columns: each register holds four consecutive codes of a row,
-                    // the low two feeding fragment 2kq and the high two fragment 2kq+1 (f16 after conversion)
-                    const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const uint32_t kbase = smem_u32(kt);
+                            for (int h = 0; h < C::kHalves; ++h)
 #pragma unroll
-                    for (int kq = 0; kq < D / 32; ++kq) {
-                        uint32_t raw[4], a[4];
-                        ldmatrix_x4(raw, kbase + tr.at(r, hp, 2 * kq + (lane >> 4)));
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
-                        mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] >> 16);
-                        mma_f16_16816(sb, a, qb[2 * kq + 1][0], qb[2 * kq + 1][1]);
-                    }
-                } else {
-                    const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const uint32_t kbase = smem_u32(kt);
-#pragma unroll
-                    for (int kk = 0; kk < KT; ++kk) {
-                        const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
-                        uint32_t a[4];
-                        ldmatrix_x4(a, kbase + tr.at(r, half, ch));
-                        if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
-                        else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+                                for (int q = 0; q < 4; ++q)
+                                    *reinterpret_cast<int4*>(vt + tr.row(r0 + 16 * c + r) +
+                                                             (hp * C::kHalves + h) * tr.half_stride +
+                                                             ((lane & 1) * 4 + q) * 16) = z;
+                        }
                     }
                 }
-                const bool vlo = (rows >> g4) & 1u, vhi = (rows >> (g4 + 8)) & 1u;
-                const float x0 = vlo ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-                const float x1 = vlo ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-                const float x2 = vhi ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-                const float x3 = vhi ? (sa[3] + sb[3]) * sl2 : -INFINITY;
-                float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+                if (zeroed) __syncwarp();
+                // S^T = K Q^T per chunk (two independent accumulation chains each)
+                float x[NC][4];
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    if (rows[c] == 0u) {
+                        x[c][0] = x[c][1] = x[c][2] = x[c][3] = -INFINITY;
+                        continue;
+                    }
+                    const int r0c = r0 + 16 * c;
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (kFp8) {
+                        // one ldmatrix.x4 per 32 e4m3 columns: each register holds four consecutive codes of a row,
+                        // the low two feeding fragment 2kq and the high two fragment 2kq+1 (f16 after conversion)
+                        const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+                        for (int kq = 0; kq < D / 32; ++kq) {
+                            uint32_t raw[4], a[4];
+                            ldmatrix_x4(raw, kbase + tr.at(r, hp, 2 * kq + (lane >> 4)));
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
+                            mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] >> 16);
+                            mma_f16_16816(sb, a, qb[2 * kq + 1][0], qb[2 * kq + 1][1]);
+                        }
+                    } else {
+                        const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
+                        const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+                        for (int kk = 0; kk < KT; ++kk) {
+                            const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
+                            uint32_t a[4];
+                            ldmatrix_x4(a, kbase + tr.at(r, half, ch));
+                            if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
+                            else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+                        }
+                    }
+                    const bool vlo = (rows[c] >> g4) & 1u, vhi = (rows[c] >> (g4 + 8)) & 1u;
+                    x[c][0] = vlo ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+                    x[c][1] = vlo ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+                    x[c][2] = vhi ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+                    x[c][3] = vhi ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+                }
+                float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+                for (int c = 1; c < NC; ++c) {
+                    mx0 = fmaxf(mx0, fmaxf(x[c][0], x[c][2]));
+                    mx1 = fmaxf(mx1, fmaxf(x[c][1], x[c][3]));
+                }
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -648,12 +677,18 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
                 const float a0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
                 const float a1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
-                const float p0 = mn0 == -INFINITY ? 0.f : fast_exp2(x0 - mn0);
-                const float p2 = mn0 == -INFINITY ? 0.f : fast_exp2(x2 - mn0);
-                const float p1 = mn1 == -INFINITY ? 0.f : fast_exp2(x1 - mn1);
-                const float p3 = mn1 == -INFINITY ? 0.f : fast_exp2(x3 - mn1);
-                l0 = l0 * a0 + p0 + p2;
-                l1 = l1 * a1 + p1 + p3;
+                float s0 = 0.f, s1 = 0.f;  // (x becomes p = 2^(x - m))
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    x[c][0] = mn0 == -INFINITY ? 0.f : fast_exp2(x[c][0] - mn0);
+                    x[c][2] = mn0 == -INFINITY ? 0.f : fast_exp2(x[c][2] - mn0);
+                    x[c][1] = mn1 == -INFINITY ? 0.f : fast_exp2(x[c][1] - mn1);
+                    x[c][3] = mn1 == -INFINITY ? 0.f : fast_exp2(x[c][3] - mn1);
+                    s0 += x[c][0] + x[c][2];
+                    s1 += x[c][1] + x[c][3];
+                }
+                l0 = l0 * a0 + s0;
+                l1 = l1 * a1 + s1;
                 m0 = mn0;
                 m1 = mn1;
 #pragma unroll
@@ -663,53 +698,54 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     o[mt][2] *= a0;
                     o[mt][3] *= a1;
                 }
-                const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
-                const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
-                if constexpr (kFp8) {
-                    // O^T += V^T P^T: ldmatrix.trans of 16-bit pairs gives a lane the codes of tokens 2c4 and
-                    // 2c4+1 at columns 2g4 and 2g4+1; a byte permutation regroups them per column, so
-                    // fragment 2kv holds the even columns of the 32-column group kv and 2kv+1 the odd ones
-                    const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
-                    const uint32_t vbase = smem_u32(vt);
 #pragma unroll
-                    for (int kv = 0; kv < D / 32; ++kv) {
-                        uint32_t raw[4], ev[4], od[4];
-                        ldmatrix_x4_trans(raw, vbase + tr.at(r, hp, 2 * kv + ((lane >> 3) & 1)));
+                for (int c = 0; c < NC; ++c) {
+                    if (rows[c] == 0u) continue;
+                    const int r0c = r0 + 16 * c;
+                    const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(x[c][0], x[c][1]) : pack_bf16x2(x[c][0], x[c][1]));
+                    const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(x[c][2], x[c][3]) : pack_bf16x2(x[c][2], x[c][3]));
+                    if constexpr (kFp8) {
+                        // O^T += V^T P^T: ldmatrix.trans of 16-bit pairs gives a lane the codes of tokens 2c4 and
+                        // 2c4+1 at columns 2g4 and 2g4+1; a byte permutation regroups them per column, so
+                        // fragment 2kv holds the even columns of the 32-column group kv and 2kv+1 the odd ones
+                        const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
+                        const uint32_t vbase = smem_u32(vt);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
-                            ev[i] = e4m3x2_to_f16x2(t & 0xFFFFu);
-                            od[i] = e4m3x2_to_f16x2(t >> 16);
+                        for (int kv = 0; kv < D / 32; ++kv) {
+                            uint32_t raw[4], ev[4], od[4];
+                            ldmatrix_x4_trans(raw, vbase + tr.at(r, hp, 2 * kv + ((lane >> 3) & 1)));
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
+                                ev[i] = e4m3x2_to_f16x2(t & 0xFFFFu);
+                                od[i] = e4m3x2_to_f16x2(t >> 16);
+                            }
+                            mma_f16_16816(o[2 * kv], ev, b0, b1);
+                            mma_f16_16816(o[2 * kv + 1], od, b0, b1);
                         }
-                        mma_f16_16816(o[2 * kv], ev, b0, b1);
-                        mma_f16_16816(o[2 * kv + 1], od, b0, b1);
-                    }
-                } else {  // O^T += V^T P^T
-                    const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
-                    const uint32_t vbase = smem_u32(vt);
+                    } else {  // O^T += V^T P^T
+                        const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
+                        const uint32_t vbase = smem_u32(vt);
 #pragma unroll
-                    for (int mt = 0; mt < KT; ++mt) {
-                        const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
-                        uint32_t a[4];
-                        ldmatrix_x4_trans(a, vbase + tr.at(r, half, ch));
-                        mma_bf16_16816(o[mt], a, b0, b1);
+                        for (int mt = 0; mt < KT; ++mt) {
+                            const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
+                            uint32_t a[4];
+                            ldmatrix_x4_trans(a, vbase + tr.at(r, half, ch));
+                            mma_bf16_16816(o[mt], a, b0, b1);
+                        }
                     }
                 }
-                if (rows != 0xFFFFu) fence_proxy_async_smem();  // zeroing before the slot's next TMA write
+                if (zeroed) fence_proxy_async_smem();  // zeroing before the slot's next TMA write
             };
-            if (inf.flags & 16) {
+            if (kPrefix && (inf.flags & 16)) {
                 // a shared-prefix item: this warp's 8 query rows against all 64 tokens of the stage (every warp
-                // zeroes the invalid V rows of a chunk before it reads them; the writes are identical)
-#pragma unroll 1
-                for (int r0c = 0; r0c < inf.ntok; r0c += 16) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
+                // zeroes the invalid V rows of a chunk before it reads them; the writes are identical).  (e4m3
+                // pools have no prefix items.)
+                if constexpr (kPrefix) chunks(std::integral_constant<int, 4>{}, 0, inf.valid);
             } else if constexpr (C::kHeads == 2) {
                 // two chunks of 16 rows of this warp's head
                 if (p.k_new) patch_new_fp8(row0, row0 + 32);
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    const int r0c = row0 + 16 * c;
-                    if (r0c < inf.ntok) chunk16(r0c, (uint32_t)(inf.valid >> r0c) & 0xFFFFu);
-                }
+                chunks(std::integral_constant<int, 2>{}, row0, inf.valid);
             } else if (row0 < inf.ntok) {
                 if (kFp8) {
                     if (p.k_new) patch_new_fp8(row0, row0 + 16);
@@ -729,14 +765,14 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     fence_proxy_async_smem();  // these writes precede the slot's next TMA write
                     __syncwarp();
                 }
-                chunk16(row0, (uint32_t)(inf.valid >> row0) & 0xFFFFu);
+                chunks(std::integral_constant<int, 1>{}, row0, inf.valid);
             }
             __syncwarp();
             if (!(inf.flags & 2)) {
                 if (lane == 0) mbar_arrive(&empty[slot]);
                 continue;
             }
-            if (inf.flags & 16) {
+            if (kPrefix && (inf.flags & 16)) {
                 // ---------------------------------------- shared-prefix item epilogue
                 // This warp's 8 rows are its own: normalise them and store every member's prefix
                 // partial (o, m, l) in workspace slot 0.  A member whose own prefix length differs
@@ -882,7 +918,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     }
 }
 
-template <int D, bool kFp8, bool kPair>
+template <int D, bool kFp8, bool kPair, bool kPrefix = false>
 int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     using C = TcCfg<D, kFp8, kPair>;
     CUtensorMap tmk, tmv;
@@ -891,7 +927,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     if ((rc = pool_tensor_map_rows(&tmv, p.v_cache, p.num_blocks, p.block_size, p.num_kv_heads, D, kFp8,
                                    C::kHeads)) != PA_OK)
         return rc;
-    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8, kPair>), C::kSmemBytes)) !=
+    if ((rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_tc_kernel<D, kFp8, kPair, kPrefix>), C::kSmemBytes)) !=
         PA_OK)
         return rc;
     // C::kCtasPerSm CTAs per SM (or as many as are resident at once, should fewer fit), never more
@@ -903,7 +939,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     int resident = resident_cache.load(std::memory_order_relaxed);
     if (resident == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8, kPair>, C::kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_tc_kernel<D, kFp8, kPair, kPrefix>, C::kThreads,
                                                           C::kSmemBytes) != cudaSuccess)
             return check_launch();
         if (n < 1) return PA_ERR_UNSUPPORTED;
@@ -913,7 +949,7 @@ int launch(const DecodeParams& p, int num_sms, cudaStream_t stream) {
     long long max_items = (long long)p.num_seqs * p.num_kv_heads * p.max_splits;
     const long long slots = (long long)num_sms * resident;
     int grid = (int)(max_items < slots ? max_items : slots);
-    return launch_kernel(decode_tc_kernel<D, kFp8, kPair>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
+    return launch_kernel(decode_tc_kernel<D, kFp8, kPair, kPrefix>, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream,
                          tmk, tmv, p, p.work);
 }
 
@@ -987,6 +1023,9 @@ int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream) {
         return PA_DECODE_FP8_PAIRS && p.num_kv_heads % 2 == 0 && p.num_seqs <= kMaxSeqsPairs
                    ? launch<128, true, true>(p, num_sms, stream)
                                                              : launch<128, true, false>(p, num_sms, stream);
+    if (p.group_offsets)  // cascade prefix items
+        return p.head_dim == 64 ? launch<64, false, false, true>(p, num_sms, stream)
+                                : launch<128, false, false, true>(p, num_sms, stream);
     return p.head_dim == 64 ? launch<64, false, false>(p, num_sms, stream)
                             : launch<128, false, false>(p, num_sms, stream);
 }
