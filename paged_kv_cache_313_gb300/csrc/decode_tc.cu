@@ -14,8 +14,11 @@
 // 64).  Items are numbered densely, sequence-major then partition then kv
 // head, from a prefix sum of the per-sequence item counts that every CTA
 // computes once from context_lens.  Persistent CTAs (two per SM; three for
-// single-head e4m3 items) take items from a global counter in the workspace,
-// so long and short sequences balance dynamically.
+// single-head e4m3 items) start on the item of their own index and take the
+// rest from a global counter in the workspace, so long and short sequences
+// balance dynamically.  The cascade's queues, which begin with shared-prefix
+// items, run on a separate instantiation (kPrefix), so that the prefix items'
+// code does not shape the plain decode kernel's.
 //
 // Inside a CTA:
 //  * Warp 4 is the producer.  For each 64-token stage it waits for a free
@@ -42,7 +45,9 @@
 //        S^T[16 tok x 8 heads] = K[16 tok x D] . Q^T        (D/16 MMAs)
 //        O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T       (D/16 MMAs)
 //    P^T goes from the accumulator layout to the B-operand layout with one
-//    movmatrix transpose per 8x8 half.  Softmax is online, in base-2 units.
+//    movmatrix transpose per 8x8 half.  Softmax is online, in base-2 units;
+//    a warp's 16-token chunks of a stage (two for two-head items, four for a
+//    shared prefix) share one step of it: one row max and one rescale of O.
 //    bf16 pools use bf16 MMAs; e4m3 pools are widened to f16 in registers
 //    (two codes per conversion) and use f16 MMAs, with the queries, already
 //    scaled, in f16.
