@@ -1028,9 +1028,8 @@ int launch_decode_tc(const DecodeParams& p, int num_sms, cudaStream_t stream) {
         return PA_DECODE_FP8_PAIRS && p.num_kv_heads % 2 == 0 && p.num_seqs <= kMaxSeqsPairs
                    ? launch<128, true, true>(p, num_sms, stream)
                                                              : launch<128, true, false>(p, num_sms, stream);
-    if (p.group_offsets)  // cascade prefix items
-        return p.head_dim == 64 ? launch<64, false, false, true>(p, num_sms, stream)
-                                : launch<128, false, false, true>(p, num_sms, stream);
+    if (p.group_offsets)  // cascade prefix items (pa_decode_cascade takes head_dim 128 only)
+        return p.head_dim == 128 ? launch<128, false, false, true>(p, num_sms, stream) : PA_ERR_UNSUPPORTED;
     return p.head_dim == 64 ? launch<64, false, false>(p, num_sms, stream)
                             : launch<128, false, false>(p, num_sms, stream);
 }
