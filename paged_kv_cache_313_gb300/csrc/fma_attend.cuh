@@ -65,23 +65,34 @@ __device__ void fma_attend(const T* __restrict__ q, int G, const T* __restrict__
             blk_s[i] = pb;
         }
         __syncthreads();
-        for (int t = warp; t < n; t += kFmaThreads / 32) {
-            const int j = c0 + t;
-            const int pb = blk_s[j / B - lb0];
-            float kr[kPerLane];
+        // two tokens per warp and round (t and t + 4), both K rows loaded before either is used
+        constexpr int kWarps = kFmaThreads / 32;
+        for (int t0 = warp; t0 < n; t0 += 2 * kWarps) {
+            float kr[2][kPerLane];
+            int pbs[2];
 #pragma unroll
-            for (int e = 0; e < kPerLane; ++e) kr[e] = 0.f;
-            if (pb >= 0) {
-                const T* krow = kc + (((size_t)pb * B + (j % B)) * Hkv + kvh) * D + lane * kPerLane;
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + u * kWarps, j = c0 + t;
+                pbs[u] = t < n ? blk_s[j / B - lb0] : -1;
 #pragma unroll
-                for (int e = 0; e < kPerLane; ++e) kr[e] = to_float(krow[e]);
+                for (int e = 0; e < kPerLane; ++e) kr[u][e] = 0.f;
+                if (pbs[u] >= 0) {
+                    const T* krow = kc + (((size_t)pbs[u] * B + (j % B)) * Hkv + kvh) * D + lane * kPerLane;
+#pragma unroll
+                    for (int e = 0; e < kPerLane; ++e) kr[u][e] = to_float(krow[e]);
+                }
             }
-            for (int g = 0; g < G; ++g) {
-                float part = 0.f;
 #pragma unroll
-                for (int e = 0; e < kPerLane; ++e) part = fmaf(q_s[g * D + lane * kPerLane + e], kr[e], part);
-                part = warp_sum(part);
-                if (lane == 0) p_s[g * kFmaSub + t] = pb >= 0 ? part * scale_log2 : -INFINITY;
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + u * kWarps;
+                if (t >= n) break;
+                for (int g = 0; g < G; ++g) {
+                    float part = 0.f;
+#pragma unroll
+                    for (int e = 0; e < kPerLane; ++e) part = fmaf(q_s[g * D + lane * kPerLane + e], kr[u][e], part);
+                    part = warp_sum(part);
+                    if (lane == 0) p_s[g * kFmaSub + t] = pbs[u] >= 0 ? part * scale_log2 : -INFINITY;
+                }
             }
         }
         __syncthreads();
@@ -112,12 +123,24 @@ __device__ void fma_attend(const T* __restrict__ q, int G, const T* __restrict__
             if (idx < G * D) {
                 const int g = idx / D, d = idx % D;
                 float a = acc[it] * alpha_s[g];
-                for (int t = 0; t < n; ++t) {
+                // eight tokens' V loads go out together, then their products are added in token order (the
+                // sum is the same as one token at a time; only the loads no longer wait on each other)
+                auto v_of = [&](int t) {
                     const int j = c0 + t;
                     const int pb = blk_s[j / B - lb0];
-                    if (pb >= 0)
-                        a = fmaf(p_s[g * kFmaSub + t], to_float(vc[(((size_t)pb * B + (j % B)) * Hkv + kvh) * D + d]), a);
+                    return pb >= 0 ? to_float(vc[(((size_t)pb * B + (j % B)) * Hkv + kvh) * D + d]) : 0.f;
+                };
+                int t = 0;
+                for (; t + 8 <= n; t += 8) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = v_of(t + u);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (blk_s[(c0 + t + u) / B - lb0] >= 0) a = fmaf(p_s[g * kFmaSub + t + u], v[u], a);
                 }
+                for (; t < n; ++t)
+                    if (blk_s[(c0 + t) / B - lb0] >= 0) a = fmaf(p_s[g * kFmaSub + t], v_of(t), a);
                 acc[it] = a;
             }
         }
