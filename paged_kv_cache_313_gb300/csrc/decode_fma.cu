@@ -15,6 +15,8 @@ namespace {
 template <typename T, int D>
 __global__ void __launch_bounds__(kFmaThreads) decode_fma_kernel(DecodeParams p) {
     using S = FmaShape<D>;
+    pdl_trigger();
+    pdl_wait();
     const int s = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
     const int G = p.group;
     const int L = decode_context(p, s, split == 0 && threadIdx.x == 0);
@@ -63,8 +65,7 @@ int launch_fma(const DecodeParams& p, cudaStream_t stream) {
     int rc = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_fma_kernel<T, D>), smem);
     if (rc != PA_OK) return rc;
     dim3 grid(p.num_seqs, p.num_kv_heads, p.max_splits);
-    decode_fma_kernel<T, D><<<grid, kFmaThreads, smem, stream>>>(p);
-    return check_launch();
+    return launch_kernel(decode_fma_kernel<T, D>, grid, dim3(kFmaThreads), smem, stream, p);
 }
 
 }  // namespace

@@ -27,6 +27,8 @@ __device__ __forceinline__ int chunk_limit(const PrefillParams& p, int c, int& s
 template <typename T, int D>
 __global__ void __launch_bounds__(kFmaThreads) prefill_fma_kernel(PrefillParams p) {
     using S = FmaShape<D>;
+    pdl_trigger();
+    pdl_wait();
     const int i = blockIdx.x, c = blockIdx.y, kvh = blockIdx.z;
     int s, start, n;
     const int cap = chunk_limit(p, c, s, start, n);
@@ -68,8 +70,7 @@ int launch(const PrefillParams& p, cudaStream_t stream) {
     int rc = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_fma_kernel<T, D>), smem);
     if (rc != PA_OK) return rc;
     dim3 grid(p.max_q_len, p.num_chunks, p.num_kv_heads);
-    prefill_fma_kernel<T, D><<<grid, kFmaThreads, smem, stream>>>(p);
-    return check_launch();
+    return launch_kernel(prefill_fma_kernel<T, D>, grid, dim3(kFmaThreads), smem, stream, p);
 }
 
 }  // namespace
