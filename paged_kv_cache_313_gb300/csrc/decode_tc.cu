@@ -624,49 +624,97 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     }
                 }
                 if (zeroed) __syncwarp();
-                // S^T = K Q^T per chunk (two independent accumulation chains each)
                 float x[NC][4];
+                bool all_active = true;  // (four-chunk path) every chunk holds a valid token
+                if constexpr (NC >= 4) {
+                    // Four chunks (the 64 tokens of a shared prefix's stage; bf16 pools only): S^T = K Q^T per
+                    // chunk (two independent accumulation chains each); with all four active the chunks advance
+                    // together, k step by k step, so that their MMA chains overlap (cascade decode 116.2 ->
+                    // 114.2 us; the same for the two chunks of an e4m3 pair item measured 1.5 us slower), else they
+                    // go one at a time.  Each chain gets the same MMAs in the same order either way.
+                    static_assert(!kFp8 || NC < 4, "shared-prefix items read bf16 pools");
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    if (rows[c] == 0u) {
-                        x[c][0] = x[c][1] = x[c][2] = x[c][3] = -INFINITY;
-                        continue;
-                    }
-                    const int r0c = r0 + 16 * c;
-                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-                    if constexpr (kFp8) {
-                        // one ldmatrix.x4 per 32 e4m3 columns: each register holds four consecutive codes of a row,
-                        // the low two feeding fragment 2kq and the high two fragment 2kq+1 (f16 after conversion)
-                        const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
-                        const uint32_t kbase = smem_u32(kt);
+                    for (int c = 0; c < NC; ++c) all_active = all_active && rows[c] != 0u;
+                    float sa[NC][4], sb[NC][4];
 #pragma unroll
-                        for (int kq = 0; kq < D / 32; ++kq) {
-                            uint32_t raw[4], a[4];
-                            ldmatrix_x4(raw, kbase + tr.at(r, hp, 2 * kq + (lane >> 4)));
+                    for (int c = 0; c < NC; ++c)
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
-                            mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
+                        for (int i = 0; i < 4; ++i) sa[c][i] = sb[c][i] = 0.f;
+                    const uint32_t kbase = smem_u32(kt);
+                    const uint32_t krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    auto qk_step = [&](int c, int kk) {  // 16 columns of chunk c: even steps into sa, odd ones into sb
+                        const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
+                        uint32_t a[4];
+                        ldmatrix_x4(a, kbase + tr.at(r0 + 16 * c + krow, half, ch));
+                        if (kk & 1) mma_bf16_16816(sb[c], a, qb[kk][0], qb[kk][1]);
+                        else mma_bf16_16816(sa[c], a, qb[kk][0], qb[kk][1]);
+                    };
+                    if (all_active) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] >> 16);
-                            mma_f16_16816(sb, a, qb[2 * kq + 1][0], qb[2 * kq + 1][1]);
-                        }
+                        for (int kk = 0; kk < KT; ++kk)
+#pragma unroll
+                            for (int c = 0; c < NC; ++c) qk_step(c, kk);
                     } else {
-                        const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
-                        const uint32_t kbase = smem_u32(kt);
 #pragma unroll
-                        for (int kk = 0; kk < KT; ++kk) {
-                            const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
-                            uint32_t a[4];
-                            ldmatrix_x4(a, kbase + tr.at(r, half, ch));
-                            if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
-                            else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+                        for (int c = 0; c < NC; ++c) {
+                            if (rows[c] == 0u) continue;
+#pragma unroll
+                            for (int kk = 0; kk < KT; ++kk) qk_step(c, kk);
                         }
                     }
-                    const bool vlo = (rows[c] >> g4) & 1u, vhi = (rows[c] >> (g4 + 8)) & 1u;
-                    x[c][0] = vlo ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-                    x[c][1] = vlo ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-                    x[c][2] = vhi ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-                    x[c][3] = vhi ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        const bool vlo = rows[c] != 0u && ((rows[c] >> g4) & 1u);
+                        const bool vhi = rows[c] != 0u && ((rows[c] >> (g4 + 8)) & 1u);
+                        x[c][0] = vlo ? (sa[c][0] + sb[c][0]) * sl2 : -INFINITY;
+                        x[c][1] = vlo ? (sa[c][1] + sb[c][1]) * sl2 : -INFINITY;
+                        x[c][2] = vhi ? (sa[c][2] + sb[c][2]) * sl2 : -INFINITY;
+                        x[c][3] = vhi ? (sa[c][3] + sb[c][3]) * sl2 : -INFINITY;
+                    }
+                } else {
+                    // S^T = K Q^T per chunk (two independent accumulation chains each)
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        if (rows[c] == 0u) {
+                            x[c][0] = x[c][1] = x[c][2] = x[c][3] = -INFINITY;
+                            continue;
+                        }
+                        const int r0c = r0 + 16 * c;
+                        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                        if constexpr (kFp8) {
+                            // one ldmatrix.x4 per 32 e4m3 columns: each register holds four consecutive codes of a row,
+                            // the low two feeding fragment 2kq and the high two fragment 2kq+1 (f16 after conversion)
+                            const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+                            for (int kq = 0; kq < D / 32; ++kq) {
+                                uint32_t raw[4], a[4];
+                                ldmatrix_x4(raw, kbase + tr.at(r, hp, 2 * kq + (lane >> 4)));
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] & 0xFFFFu);
+                                mma_f16_16816(sa, a, qb[2 * kq][0], qb[2 * kq][1]);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) a[i] = e4m3x2_to_f16x2(raw[i] >> 16);
+                                mma_f16_16816(sb, a, qb[2 * kq + 1][0], qb[2 * kq + 1][1]);
+                            }
+                        } else {
+                            const uint32_t r = r0c + (lane & 7) + ((lane >> 3) & 1) * 8;
+                            const uint32_t kbase = smem_u32(kt);
+#pragma unroll
+                            for (int kk = 0; kk < KT; ++kk) {
+                                const uint32_t half = kk >> 2, ch = (kk & 3) * 2 + (lane >> 4);
+                                uint32_t a[4];
+                                ldmatrix_x4(a, kbase + tr.at(r, half, ch));
+                                if (kk & 1) mma_bf16_16816(sb, a, qb[kk][0], qb[kk][1]);
+                                else mma_bf16_16816(sa, a, qb[kk][0], qb[kk][1]);
+                            }
+                        }
+                        const bool vlo = (rows[c] >> g4) & 1u, vhi = (rows[c] >> (g4 + 8)) & 1u;
+                        x[c][0] = vlo ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+                        x[c][1] = vlo ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+                        x[c][2] = vhi ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+                        x[c][3] = vhi ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+                    }
                 }
                 float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
@@ -703,40 +751,73 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                     o[mt][2] *= a0;
                     o[mt][3] *= a1;
                 }
+                if constexpr (NC >= 4) {
+                    // O^T += V^T P^T for four chunks, advancing together when all are active (as the scores above)
+                    uint32_t pb0[NC], pb1[NC];  // P^T of each chunk in the B-operand layout
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    if (rows[c] == 0u) continue;
-                    const int r0c = r0 + 16 * c;
-                    const uint32_t b0 = movmatrix_trans(kFp8 ? pack_f16x2(x[c][0], x[c][1]) : pack_bf16x2(x[c][0], x[c][1]));
-                    const uint32_t b1 = movmatrix_trans(kFp8 ? pack_f16x2(x[c][2], x[c][3]) : pack_bf16x2(x[c][2], x[c][3]));
-                    if constexpr (kFp8) {
-                        // O^T += V^T P^T: ldmatrix.trans of 16-bit pairs gives a lane the codes of tokens 2c4 and
-                        // 2c4+1 at columns 2g4 and 2g4+1; a byte permutation regroups them per column, so
-                        // fragment 2kv holds the even columns of the 32-column group kv and 2kv+1 the odd ones
-                        const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
-                        const uint32_t vbase = smem_u32(vt);
+                    for (int c = 0; c < NC; ++c) {
+                        pb0[c] = movmatrix_trans(pack_bf16x2(x[c][0], x[c][1]));
+                        pb1[c] = movmatrix_trans(pack_bf16x2(x[c][2], x[c][3]));
+                    }
+                    const uint32_t vbase = smem_u32(vt);
+                    const uint32_t vrow = (lane & 7) + (lane >> 4) * 8;
+                    auto pv_step = [&](int c, int mt) {  // 16 output columns from chunk c
+                        const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
+                        uint32_t a[4];
+                        ldmatrix_x4_trans(a, vbase + tr.at(r0 + 16 * c + vrow, half, ch));
+                        mma_bf16_16816(o[mt], a, pb0[c], pb1[c]);
+                    };
+                    if (all_active) {
 #pragma unroll
-                        for (int kv = 0; kv < D / 32; ++kv) {
-                            uint32_t raw[4], ev[4], od[4];
-                            ldmatrix_x4_trans(raw, vbase + tr.at(r, hp, 2 * kv + ((lane >> 3) & 1)));
+                        for (int mt = 0; mt < KT; ++mt)
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
-                                ev[i] = e4m3x2_to_f16x2(t & 0xFFFFu);
-                                od[i] = e4m3x2_to_f16x2(t >> 16);
-                            }
-                            mma_f16_16816(o[2 * kv], ev, b0, b1);
-                            mma_f16_16816(o[2 * kv + 1], od, b0, b1);
+                            for (int c = 0; c < NC; ++c) pv_step(c, mt);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            if (rows[c] == 0u) continue;
+#pragma unroll
+                            for (int mt = 0; mt < KT; ++mt) pv_step(c, mt);
                         }
-                    } else {  // O^T += V^T P^T
-                        const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
-                        const uint32_t vbase = smem_u32(vt);
+                    }
+                } else {
 #pragma unroll
-                        for (int mt = 0; mt < KT; ++mt) {
-                            const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
-                            uint32_t a[4];
-                            ldmatrix_x4_trans(a, vbase + tr.at(r, half, ch));
-                            mma_bf16_16816(o[mt], a, b0, b1);
+                    for (int c = 0; c < NC; ++c) {
+                        if (rows[c] == 0u) continue;
+                        const int r0c = r0 + 16 * c;
+                        const uint32_t b0 =
+                            movmatrix_trans(kFp8 ? pack_f16x2(x[c][0], x[c][1]) : pack_bf16x2(x[c][0], x[c][1]));
+                        const uint32_t b1 =
+                            movmatrix_trans(kFp8 ? pack_f16x2(x[c][2], x[c][3]) : pack_bf16x2(x[c][2], x[c][3]));
+                        if constexpr (kFp8) {
+                            // O^T += V^T P^T: ldmatrix.trans of 16-bit pairs gives a lane the codes of tokens 2c4 and
+                            // 2c4+1 at columns 2g4 and 2g4+1; a byte permutation regroups them per column, so
+                            // fragment 2kv holds the even columns of the 32-column group kv and 2kv+1 the odd ones
+                            const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
+                            const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+                            for (int kv = 0; kv < D / 32; ++kv) {
+                                uint32_t raw[4], ev[4], od[4];
+                                ldmatrix_x4_trans(raw, vbase + tr.at(r, hp, 2 * kv + ((lane >> 3) & 1)));
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const uint32_t t = __byte_perm(raw[i], 0u, 0x3120);
+                                    ev[i] = e4m3x2_to_f16x2(t & 0xFFFFu);
+                                    od[i] = e4m3x2_to_f16x2(t >> 16);
+                                }
+                                mma_f16_16816(o[2 * kv], ev, b0, b1);
+                                mma_f16_16816(o[2 * kv + 1], od, b0, b1);
+                            }
+                        } else {  // O^T += V^T P^T
+                            const uint32_t r = r0c + (lane & 7) + (lane >> 4) * 8;
+                            const uint32_t vbase = smem_u32(vt);
+#pragma unroll
+                            for (int mt = 0; mt < KT; ++mt) {
+                                const uint32_t half = mt >> 2, ch = (mt & 3) * 2 + ((lane >> 3) & 1);
+                                uint32_t a[4];
+                                ldmatrix_x4_trans(a, vbase + tr.at(r, half, ch));
+                                mma_bf16_16816(o[mt], a, b0, b1);
+                            }
                         }
                     }
                 }
