@@ -67,6 +67,7 @@
 // memory when the CTA is gone.  The work counter is reset by the last CTA to
 // finish.
 #include <atomic>
+#include <climits>
 #include <type_traits>
 
 #include "decode_common.cuh"
@@ -150,8 +151,8 @@ struct TcCfg {
     static constexpr int kScan = kRed + kRedBytes;
     static constexpr int kInfo = kScan + 64;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
-    // full[kStages], empty[kStages], and the consumers' epilogue barrier
-    static constexpr int kCtx = kBars + (2 * kStages + 1) * 8;
+    // full[kStages], empty[kStages], the consumers' epilogue barrier and the prefix sum's completion
+    static constexpr int kCtx = kBars + (2 * kStages + 2) * 8;
     // an SM holds 228 KiB of shared memory, 1 KiB of it reserved per resident CTA, and 1 KiB of each CTA's
     // allocation goes to aligning the base; every array lives in the dynamic allocation
     static constexpr int kSmemCap = 228 * 1024 / kCtasPerSm - 2 * 1024;
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBars);
     uint64_t* empty = full + C::kStages;
     uint64_t* cons_bar = empty + C::kStages;  // the consumer warps' epilogue barrier (bounded)
+    uint64_t* cum_bar = cons_bar + 1;         // the consumers' prefix sum (cum, ctx, s_total) is written
     auto red_m = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed);
     auto red_l = reinterpret_cast<float(*)[C::kConsumerWarps][8]>(smem + C::kRed + C::kRedBytes / 2);
     int* warp_tot = reinterpret_cast<int*>(smem + C::kScan);
@@ -221,15 +223,35 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], C::kConsumerWarps);
+        }
+        mbar_init(cons_bar, C::kConsumerWarps);
+        mbar_init(cum_bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
 
-    // ---- per-sequence item counts and their exclusive prefix sum (every CTA, once).  (Queueing
-    // every sequence's short last partition after all the whole ones was measured 5-7% slower.)
+    // ---- Item numbering.  Plain decode: items [0, N*HkvI) are the partition-0 items, (sequence i / HkvI,
+    // kv head slot i % HkvI), numbered without any table, so that a CTA's first copies wait only for its own
+    // sequence's context length and table entries; then the (sequence, partition >= 1, kv head slot) items
+    // through the exclusive prefix sum cum[] of the per-sequence counts of those.  The cascade's kernel
+    // numbers every (sequence, partition, kv head) item through cum[], after its groups' prefix items.
+    // The consumer warps compute cum[] (and the clamped context lengths) while the producer starts its
+    // first item, and signal cum_bar when it is written.  (Queueing every sequence's short last partition
+    // after all the whole ones was measured 5-7% slower.)
+    constexpr bool kDirect = !kPrefix;
+    const int n_first = kDirect ? N * HkvI : 0;  // items numbered directly
     auto counted_items = [&](int L, int s) {
         int pre;
-        return num_partitions(L - decode_start(p, s, L, &pre), partition_of(p, s)) * HkvI;
+        return (num_partitions(L - decode_start(p, s, L, &pre), partition_of(p, s)) - (kDirect ? 1 : 0)) * HkvI;
     };
-    {
-        const int per = (N + C::kThreads - 1) / C::kThreads;
+    if (warp < C::kConsumerWarps) {
+        constexpr int kScanThreads = C::kConsumerWarps * 32;
+        auto consumer_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads) : "memory"); };
+        const int per = (N + kScanThreads - 1) / kScanThreads;
         const int first = threadIdx.x * per;
         int local = 0;
         for (int i = 0; i < per && first + i < N; ++i)
@@ -241,15 +263,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             if (lane >= off) incl += v;
         }
         if (lane == 31) warp_tot[warp] = incl;
-        if (threadIdx.x == 0) {
-            for (int i = 0; i < C::kStages; ++i) {
-                mbar_init(&full[i], 1);
-                mbar_init(&empty[i], C::kConsumerWarps);
-            }
-            mbar_init(cons_bar, C::kConsumerWarps);
-            fence_mbar_init();
-        }
-        __syncthreads();
+        consumer_sync();
         int run = incl - local;
         for (int w = 0; w < warp; ++w) run += warp_tot[w];
         for (int i = 0; i < per && first + i < N; ++i) {
@@ -258,18 +272,18 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             if (C::kCtxN) ctx[first + i] = L;
             run += counted_items(L, first + i);
         }
-        if (threadIdx.x == C::kThreads - 1) {
+        if (threadIdx.x == kScanThreads - 1) {
             int tot = 0;
-            for (int w = 0; w < C::kThreads / 32; ++w) tot += warp_tot[w];
+            for (int w = 0; w < C::kConsumerWarps; ++w) tot += warp_tot[w];
             s_total = tot;
             cum[N] = tot;
         }
-        __syncthreads();
+        consumer_sync();
+        if (threadIdx.x == 0) mbar_arrive(cum_bar);  // releases every consumer's writes (ordered by the barrier)
     }
     // items: the cascade groups' shared prefixes (one per group and kv head) first, then the
-    // (sequence, partition, kv head) items of the prefix sum
+    // (sequence, partition, kv head) items
     const int n_grouped = kPrefix && p.group_offsets ? p.num_groups * Hkv : 0;
-    const int total = n_grouped + s_total;
 
     if (warp == C::kConsumerWarps) {
         // ================================================================ producer
@@ -311,9 +325,19 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 d.ntok = pre;
                 d.L = 0;
             } else {
-                decode_item(cum, N, HkvI, it - n_grouped, d.s, d.split, d.kvh);
+                const int i = it - n_grouped;
+                if (i < n_first) {  // a partition-0 item (its context length read from global memory: the
+                                    // shared-memory copy may not be written yet)
+                    d.s = i / HkvI;
+                    d.split = 0;
+                    d.kvh = i - d.s * HkvI;
+                    d.L = decode_context(p, d.s, false);
+                } else {
+                    decode_item(cum, N, HkvI, i - n_first, d.s, d.split, d.kvh);
+                    d.split += kDirect ? 1 : 0;
+                    d.L = context_of(d.s);
+                }
                 d.kvh *= C::kHeads;  // the item's first kv head
-                d.L = context_of(d.s);
                 const int j_first = decode_start(p, d.s, d.L, &d.pre);
                 const int part = partition_of(p, d.s);
                 d.nsplit = num_partitions(d.L - j_first, part);
@@ -337,21 +361,33 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
         // the counter's places after the grid's
         int item = blockIdx.x;
         int nxt = 0;  // the item after this one (lane 0), claimed a few stages before this one's last
+        bool ok = true;
+        // the item count, known once the consumers' prefix sum is in; items below n_grouped + n_first exist
+        // without it
+        int total = -1;
+        auto is_item = [&](int it) {
+            if (it < n_grouped + n_first) return true;
+            if (total < 0) {
+                total = 0;
+                if (mbar_wait_warp(cum_bar, 0)) total = n_grouped + n_first + s_total;
+                else ok = false;
+            }
+            return it < total;
+        };
         Item d{};
         int raw = -1;
-        if (item < total) {
+        if (is_item(item)) {
             d = describe(item);
             raw = load_chunk(d, 0);
         }
         uint32_t stage_no = 0;  // stages issued by this CTA
-        bool ok = true;
-        while (item < total && ok) {
+        while (ok && is_item(item)) {
             const int nst = max(1, (d.ntok + C::kStageTok - 1) / C::kStageTok);
             const int nblk = (d.ntok + B - 1) / B;
             int pb_lane = -1;                 // physical block of this lane's table entry in the current chunk
             unsigned long long lvalid = 0ull; // lane l: valid-token mask of the chunk's stage l
             int lnvb = 0;                     // and how many of its blocks are loaded
-            int item2 = total, raw2 = -1;
+            int item2 = INT_MAX, raw2 = -1;
             Item d2{};
             // The next item is claimed when PA_DECODE_CLAIM_STAGES stages of this one are left to issue and
             // described (with its first table chunk loaded) one stage later, so the claim's latency is hidden
@@ -464,7 +500,7 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
                 if (st == claim_at && lane == 0) nxt = (int)gridDim.x + atomicAdd(&work[0], 1);
                 if (st == describe_at) {
                     item2 = __shfl_sync(0xffffffffu, nxt, 0);
-                    if (item2 < total) {
+                    if (is_item(item2)) {
                         d2 = describe(item2);
                         raw2 = load_chunk(d2, 0);
                     }
