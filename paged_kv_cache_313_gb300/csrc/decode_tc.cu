@@ -11,9 +11,11 @@
 // kv head) — or, for e4m3 pools with an even number of kv heads, a pair of
 // adjacent kv heads, whose rows sit side by side in the pool so that one box
 // per block carries both; partitions are `partition` tokens (a multiple of
-// 64).  Items are numbered densely, sequence-major then partition then kv
-// head, from a prefix sum of the per-sequence item counts that every CTA
-// computes once from context_lens.  Persistent CTAs (two per SM; three for
+// 64).  Items are numbered densely: first partition 0 of every (sequence, kv
+// head), numbered directly, then the later partitions sequence-major then
+// partition then kv head, through a prefix sum of the per-sequence counts
+// that every CTA's consumer warps compute once from context_lens while its
+// producer starts on its first item.  Persistent CTAs (two per SM; three for
 // single-head e4m3 items) start on the item of their own index and take the
 // rest from a global counter in the workspace, so long and short sequences
 // balance dynamically.  The cascade's queues, which begin with shared-prefix
