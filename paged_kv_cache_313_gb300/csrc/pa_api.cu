@@ -1,6 +1,7 @@
 // pa_api.cu — the C ABI of libpa.so: argument checks, device checks and
 // dispatch to the kernels.  Every entry point validates on the host and
 // launches nothing when a check fails.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -85,9 +86,13 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 // Items per SM below which decode partitions shrink from 512 to 256 and 128
 // tokens (build-time knob; 0, the measured best, keeps 512 whenever the grid
 // covers two waves: shorter items spend more of their time in the epilogue).
-// Decode partition (tokens per work item) before any shrinking or growing.
+// Decode partition (tokens per work item) before any shrinking or growing: bf16 pools, and e4m3 pools (whose
+// items carry two kv heads).  768 for bf16 measured against 512, 1024 (the e4m3 best) and 1280.
 #ifndef PA_DECODE_PARTITION
-#define PA_DECODE_PARTITION 1024
+#define PA_DECODE_PARTITION 768
+#endif
+#ifndef PA_DECODE_PARTITION_FP8
+#define PA_DECODE_PARTITION_FP8 1024
 #endif
 #ifndef PA_DECODE_ITEMS_PER_SM
 #define PA_DECODE_ITEMS_PER_SM 0
@@ -100,7 +105,7 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 #endif
 
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
-                       int num_sms, size_t workspace_cap, int reserved) {
+                       int num_sms, size_t workspace_cap, int reserved, bool fp8) {
     // Work items are (sequence, partition, kv head).  PA_DECODE_PARTITION-token
     // partitions (1024: measured against 512 and 2048, it halves the partials
     // a long context leaves to merge and is neutral elsewhere) keep each item's
@@ -114,9 +119,11 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         long long splits = ((long long)max_context_len + part - 1) / part;
         return (long long)num_seqs * num_kv_heads * (splits < 1 ? 1 : splits);
     };
-    int partition = PA_DECODE_PARTITION;
-    while (partition > 128 && items(partition) < (long long)PA_DECODE_ITEMS_PER_SM * num_sms) partition >>= 1;
-    while (partition > 64 && items(partition) < 2LL * num_sms) partition >>= 1;
+    // (halving keeps a multiple of 64)
+    auto half_of = [](int part) { return std::max(64, (part >> 1) & ~63); };
+    int partition = fp8 ? PA_DECODE_PARTITION_FP8 : PA_DECODE_PARTITION;
+    while (partition > 128 && items(partition) < (long long)PA_DECODE_ITEMS_PER_SM * num_sms) partition = half_of(partition);
+    while (partition > 64 && items(partition) < 2LL * num_sms) partition = half_of(partition);
     auto splits_of = [&](int part) {
         int sp = (int)(((long long)max_context_len + part - 1) / part);
         return sp < 1 ? 1 : sp;
@@ -124,7 +131,7 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
     // the last sequences (PA_DECODE_SMALL_TAIL_PCT % of them, rounded up) use quarter-length partitions, as
     // long as their items, counted at the longest context, stay within four per resident CTA (two per SM):
     // a few long contexts cut small would add more per-item work than the shorter tail saves
-    auto small_of = [](int part) { return part / 4 < 64 ? 64 : part / 4; };
+    auto small_of = [](int part) { return std::max(64, (part / 4) & ~63); };
     const long long small_items_per_seq = (long long)splits_of(small_of(partition)) * num_kv_heads;
     long long small_count = ((long long)num_seqs * PA_DECODE_SMALL_TAIL_PCT + 99) / 100;
     if (small_count * small_items_per_seq > 8LL * num_sms) small_count = 8LL * num_sms / small_items_per_seq;
@@ -294,8 +301,14 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
         return 0;
     int num_sms = 0;
     if (check_device(&num_sms) != PA_OK) return 0;
-    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX);
-    return decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total;
+    // enough for bf16 and for e4m3 pools, whose plans differ
+    size_t total = 0;
+    for (bool fp8 : {false, true}) {
+        DecodePlan plan =
+            plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, num_sms, SIZE_MAX, 0, fp8);
+        total = std::max(total, decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits).total);
+    }
+    return total;
 }
 
 int pa_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
@@ -317,7 +330,7 @@ static int prepare_decode(DecodeParams* p, int* num_sms, void* out, const void* 
                           int num_kv_heads, int head_dim, int dtype, const void* k_cache, const void* v_cache,
                           int num_blocks, int block_size, const int32_t* block_tables, int max_blocks_per_seq,
                           const int32_t* context_lens, int max_context_len, float scale, void* workspace,
-                          size_t workspace_bytes, int32_t* error_count) {
+                          size_t workspace_bytes, int32_t* error_count, bool fp8 = false) {
     if (num_seqs < 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
     int rc = decode_shape_ok(num_q_heads, num_kv_heads, head_dim, block_size);
     if (rc != PA_OK) return rc;
@@ -325,7 +338,8 @@ static int prepare_decode(DecodeParams* p, int* num_sms, void* out, const void* 
     if (!out || !q || !k_cache || !v_cache || !context_lens || (max_blocks_per_seq > 0 && !block_tables))
         return PA_ERR_INVALID_ARG;
     if ((rc = check_device(num_sms)) != PA_OK) return rc;
-    DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, *num_sms, SIZE_MAX);
+    DecodePlan plan =
+        plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, *num_sms, SIZE_MAX, 0, fp8);
     DecodeWorkspace lay = decode_workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_splits);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PA_ERR_WORKSPACE;
@@ -388,7 +402,7 @@ int pa_decode_fp8(void* out, const void* q, int num_seqs, int num_q_heads, int n
     int num_sms = 0;
     int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, PA_BF16, k_cache,
                             v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
-                            max_context_len, scale, workspace, workspace_bytes, error_count);
+                            max_context_len, scale, workspace, workspace_bytes, error_count, true);
     if (rc != PA_OK) return rc;
     p.kv_fp8 = 1;
     p.k_scale = k_scale;
@@ -439,7 +453,7 @@ int pa_decode_write_fp8(void* out, const void* q, int num_seqs, int num_q_heads,
     int num_sms = 0;
     int rc = prepare_decode(&p, &num_sms, out, q, num_seqs, num_q_heads, num_kv_heads, head_dim, PA_BF16, k_cache,
                             v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq, context_lens,
-                            max_context_len, scale, workspace, workspace_bytes, error_count);
+                            max_context_len, scale, workspace, workspace_bytes, error_count, true);
     if (rc != PA_OK) return rc;
     p.kv_fp8 = 1;
     p.k_scale = k_scale;

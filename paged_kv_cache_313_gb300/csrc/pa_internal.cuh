@@ -62,9 +62,10 @@ struct DecodePlan {
     int small_from;       // first sequence cut into small_partition-token partitions (num_seqs: none)
 };
 // `workspace_cap`: largest split-KV scratch the caller can offer (SIZE_MAX: any); `reserved`: partial slots
-// per (sequence, kv head) used before the partitions' (the cascade's prefix slot).
+// per (sequence, kv head) used before the partitions' (the cascade's prefix slot); `fp8`: the plan of e4m3
+// pools (pa_decode_fp8, pa_decode_write_fp8).
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
-                       int num_sms, size_t workspace_cap, int reserved = 0);
+                       int num_sms, size_t workspace_cap, int reserved = 0, bool fp8 = false);
 
 // Workspace layout of pa_decode (byte offsets from the 256-aligned base).
 struct DecodeWorkspace {

@@ -68,7 +68,7 @@ def test_noalloc_matches_oracle_twice(name):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_noalloc_lengthens_partitions_to_fit_its_scratch(dtype):
     """512 sequences of one kv head with 8 query heads and contexts up to 8192 tokens: pa_decode's plan
-    (1024-token partitions) needs more scratch, more than the 16 MiB array holds, so
+    (768-token partitions) needs more scratch, more than the 16 MiB array holds, so
     this call succeeds only with longer partitions (pa_decode's plan also reserves room for the quarter-length partitions of the batch's last sequences).  Block tables draw their entries from a pool of 700 blocks
     (a block may appear in several tables), which keeps the pool small."""
     rng = np.random.default_rng(31)
