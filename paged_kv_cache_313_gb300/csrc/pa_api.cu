@@ -103,6 +103,13 @@ DecodeWorkspace decode_workspace_layout(int num_seqs, int num_q_heads, int num_k
 #ifndef PA_DECODE_SMALL_TAIL_PCT
 #define PA_DECODE_SMALL_TAIL_PCT 20
 #endif
+// The most quarter-length items (counted at the longest context) per SM: bf16 pools, e4m3 pools.
+#ifndef PA_DECODE_SMALL_TAIL_ITEMS
+#define PA_DECODE_SMALL_TAIL_ITEMS 8
+#endif
+#ifndef PA_DECODE_SMALL_TAIL_ITEMS_FP8
+#define PA_DECODE_SMALL_TAIL_ITEMS_FP8 12
+#endif
 
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
                        int num_sms, size_t workspace_cap, int reserved, bool fp8) {
@@ -129,12 +136,14 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         return sp < 1 ? 1 : sp;
     };
     // the last sequences (PA_DECODE_SMALL_TAIL_PCT % of them, rounded up) use quarter-length partitions, as
-    // long as their items, counted at the longest context, stay within four per resident CTA (two per SM):
-    // a few long contexts cut small would add more per-item work than the shorter tail saves
+    // long as their items, counted at the longest context, stay within four per resident CTA on bf16 pools
+    // (six on e4m3 pools, whose longer items leave a coarser tail): a few long contexts cut small would add
+    // more per-item work than the shorter tail saves
     auto small_of = [](int part) { return std::max(64, (part / 4) & ~63); };
     const long long small_items_per_seq = (long long)splits_of(small_of(partition)) * num_kv_heads;
+    const long long small_cap = (fp8 ? PA_DECODE_SMALL_TAIL_ITEMS_FP8 : PA_DECODE_SMALL_TAIL_ITEMS) * (long long)num_sms;
     long long small_count = ((long long)num_seqs * PA_DECODE_SMALL_TAIL_PCT + 99) / 100;
-    if (small_count * small_items_per_seq > 8LL * num_sms) small_count = 8LL * num_sms / small_items_per_seq;
+    if (small_count * small_items_per_seq > small_cap) small_count = small_cap / small_items_per_seq;
     auto slots_of = [&](int part) {  // partial slots per (sequence, kv head)
         return reserved + (small_count > 0 ? splits_of(small_of(part)) : splits_of(part));
     };
