@@ -171,6 +171,36 @@ def test_split_count_does_not_change_the_result(dtype, tol):
     assert float((alone[0].float() - batch[5].float()).abs().max()) <= tol
 
 
+@pytest.mark.parametrize("N", [2, 4, 6])
+def test_small_batches_shrink_partitions_in_multiples_of_64(N):
+    """Small bf16 batches: the plan halves the partitions until the items cover the GPU twice (768 -> 384 ->
+    192 -> 64 tokens, every length and its quarter-length tail a multiple of 64), and the decode still
+    matches the oracle."""
+    rng = np.random.default_rng(40 + N)
+    Hq, Hkv, D, B = 32, 8, 128, 16
+    lens = rng.integers(2500, 4097, size=N).astype(np.int32)
+    part, splits = pa.pa_decode_plan(N, Hq, Hkv, D, B, int(lens.max()))
+    assert part % 64 == 0 and part < 768 and splits >= -(-int(lens.max()) // part)
+    nblk = [oracle.num_blocks(int(L), B) for L in lens]
+    P = sum(nblk) + 11
+    perm = rng.permutation(P).astype(np.int32)
+    width = max(nblk)
+    bt = np.full((N, width), -1, np.int32)
+    o = 0
+    for i, n in enumerate(nblk):
+        bt[i, :n] = perm[o:o + n]
+        o += n
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16)  # noqa: E731
+    q, kc, vc = (bf(rng.standard_normal(sh, dtype=np.float32)) for sh in ((N, Hq, D), (P, B, Hkv, D), (P, B, Hkv, D)))
+    want = oracle.decode(storage_numpy(q), storage_numpy(kc), storage_numpy(vc), bt, lens, 1 / math.sqrt(D))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _decode_direct(q.cuda(), kc.cuda(), vc.cuda(), torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda(),
+                         int(lens.max()), 1 / math.sqrt(D), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _maxabs(got, want) <= TOL[torch.bfloat16]
+
+
 def test_empty_and_single_token_contexts():
     rng = np.random.default_rng(3)
     P, B, Hq, Hkv, D = 8, 16, 8, 2, 128
