@@ -86,8 +86,13 @@ namespace {
 #ifndef PA_DECODE_KV_EVICT_FIRST
 #define PA_DECODE_KV_EVICT_FIRST 1
 #endif
+// How many stages before an item's last one the producer claims the next item: bf16 pools, e4m3 pools
+// (measured against 1, 2 and 3 for each).
 #ifndef PA_DECODE_CLAIM_STAGES
-#define PA_DECODE_CLAIM_STAGES 2
+#define PA_DECODE_CLAIM_STAGES 3
+#endif
+#ifndef PA_DECODE_CLAIM_STAGES_FP8
+#define PA_DECODE_CLAIM_STAGES_FP8 1
 #endif
 // e4m3 pools with an even number of kv heads: items of two kv heads.
 #ifndef PA_DECODE_FP8_PAIRS
@@ -391,10 +396,11 @@ __global__ void __launch_bounds__(TcCfg<D, kFp8, kPair>::kThreads, TcCfg<D, kFp8
             int lnvb = 0;                     // and how many of its blocks are loaded
             int item2 = INT_MAX, raw2 = -1;
             Item d2{};
-            // The next item is claimed when PA_DECODE_CLAIM_STAGES stages of this one are left to issue and
+            // The next item is claimed when kClaimStages stages of this one are left to issue and
             // described (with its first table chunk loaded) one stage later, so the claim's latency is hidden
             // while a CTA never holds more than the rest of one item when the queue runs dry.
-            const int claim_at = max(0, nst - PA_DECODE_CLAIM_STAGES), describe_at = min(nst - 1, claim_at + 1);
+            constexpr int kClaimStages = kFp8 ? PA_DECODE_CLAIM_STAGES_FP8 : PA_DECODE_CLAIM_STAGES;
+            const int claim_at = max(0, nst - kClaimStages), describe_at = min(nst - 1, claim_at + 1);
             for (int st = 0; st < nst; ++st) {
                 const int slot = stage_no % C::kStages;
                 const int chunk = st / spc, l = st - chunk * spc;
